@@ -1,0 +1,40 @@
+"""GB300 (sm_103a) fused attention forward: Python binding over libfa_gb300.so.
+
+Argument marshalling only — every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/fa.h``.  PyTorch supplies device
+memory and streams.  There is no CPU fallback: when the library is missing or
+the device is not sm_103, calls raise.
+
+Entry points (same names as the C ABI):
+
+* ``fa_fwd(q, k, v, ...)``         padded-batch prefill   q [B, Nq, Hq, d]
+* ``fa_fwd_varlen(q, k, v, ...)``  packed varlen prefill  q [total_q, Hq, d]
+* ``fa_decode(q, k_cache, v_cache, seqlens_k, ...)``  one new token per sequence
+* ``fa_device_status()``           read/clear the kernels' error word
+"""
+
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    FAError,
+    decode_workspace_size,
+    fa_decode,
+    fa_decode_max_splits,
+    fa_device_status,
+    fa_fwd,
+    fa_fwd_varlen,
+    library_path,
+    load_library,
+)
+
+__all__ = [
+    "FAError",
+    "fa_fwd",
+    "fa_fwd_varlen",
+    "fa_decode",
+    "fa_decode_max_splits",
+    "decode_workspace_size",
+    "fa_device_status",
+    "load_library",
+    "library_path",
+]

@@ -1,0 +1,197 @@
+"""ctypes binding of libfa_gb300.so (see include/fa.h for the contracts)."""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
+
+_SIGS = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp]),
+    "fa_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _ip,
+                           _vp]),
+    "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp, _sz, _vp]),
+    "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _ip, _i]),
+    "fa_last_error": (ctypes.c_char_p, []),
+    "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise FAError(FA_ERR_UNSUPPORTED,
+                              f"{_LIB_PATH} is missing; build it with "
+                              "`python -m flashattention_forward_fa_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != FA_OK:
+        raise FAError(status, load_library().fa_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _host_ints(x) -> Optional[ctypes.Array]:
+    if x is None:
+        return None
+    vals = [int(v) for v in (x.tolist() if isinstance(x, torch.Tensor) else x)]
+    return (ctypes.c_int * len(vals))(*vals)
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise FAError(FA_ERR_INVALID, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise FAError(FA_ERR_INVALID, f"{name} must be {dtype}")
+    if not t.is_contiguous():
+        raise FAError(FA_ERR_INVALID, f"{name} must be contiguous")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, window: int = 0,
+           scale: Optional[float] = None, seqlens_q: Optional[torch.Tensor] = None,
+           seqlens_k: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, return_lse: bool = True
+           ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Padded-batch prefill.  q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d] bf16 -> (O, LSE [B, Hq, Nq])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise FAError(FA_ERR_INVALID, "expected q [B,Nq,Hq,d] and k, v [B,Nk,Hkv,d]")
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    if k.shape[0] != B or k.shape[3] != d:
+        raise FAError(FA_ERR_INVALID, "q and k disagree on B or d")
+    for t, n in ((seqlens_q, "seqlens_q"), (seqlens_k, "seqlens_k")):
+        if t is not None:
+            _need(t, n, torch.int32)
+    o = out if out is not None else torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, sc,
+                      int(bool(causal)), int(window), _ptr(seqlens_q), _ptr(seqlens_k), _stream(q)))
+    return o, lse
+
+
+def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                  cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
+                  window: int = 0, scale: Optional[float] = None, cu_seqlens_q_host: Optional[Sequence[int]] = None,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Packed varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] -> (O, LSE [Hq, total_q])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise FAError(FA_ERR_INVALID, "expected q [total_q,Hq,d] and k, v [total_k,Hkv,d]")
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if B <= 0 or cu_seqlens_k.numel() != B + 1:
+        raise FAError(FA_ERR_INVALID, "cu_seqlens_q/k must both have B + 1 entries")
+    o = out if out is not None else torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    host = _host_ints(cu_seqlens_q_host)
+    _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, total_q, total_k,
+                             int(max_seqlen_q), int(max_seqlen_k), d, sc, int(bool(causal)), int(window),
+                             _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                             ctypes.cast(host, _ip) if host is not None else None, _stream(q)))
+    return o, lse
+
+
+def decode_workspace_size(B: int, Hq: int, d: int, max_splits: int) -> int:
+    return int(load_library().fa_decode_workspace_size(B, Hq, d, max_splits))
+
+
+def fa_decode_max_splits(B: int, Hq: int, Hkv: int, Ncap: int, window: int = 0, seqlens_k_host=None,
+                         num_splits: int = 0) -> int:
+    host = _host_ints(seqlens_k_host)
+    return int(load_library().fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window),
+                                                   ctypes.cast(host, _ip) if host is not None else None,
+                                                   int(num_splits)))
+
+
+def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens_k: torch.Tensor,
+              window: int = 0, scale: Optional[float] = None, num_splits: int = 0, seqlens_k_host=None,
+              workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+              lse: Optional[torch.Tensor] = None, return_lse: bool = True
+              ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode: q [B, Hq, d], caches [B, Ncap, Hkv, d], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
+    lib = load_library()
+    _need(q, "q")
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    _need(seqlens_k, "seqlens_k", torch.int32)
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise FAError(FA_ERR_INVALID, "expected q [B,Hq,d] and caches [B,Ncap,Hkv,d]")
+    B, Hq, d = q.shape
+    _, Ncap, Hkv, _ = k_cache.shape
+    host = _host_ints(seqlens_k_host)
+    hostp = ctypes.cast(host, _ip) if host is not None else None
+    if workspace is None:
+        S = lib.fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window), hostp, int(num_splits))
+        nbytes = lib.fa_decode_workspace_size(B, Hq, d, max(S, 1))
+        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=q.device)
+    o = out if out is not None else torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
+                         int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(q)))
+    return o, lse
+
+
+def fa_device_status(clear: bool = True) -> int:
+    """Synchronise and return the kernels' error bits (0 = clean)."""
+    bits = ctypes.c_uint32(0)
+    load_library().fa_device_status(ctypes.byref(bits), int(bool(clear)))
+    return int(bits.value)

@@ -1,0 +1,350 @@
+// C-ABI layer of libfa_gb300: argument checks, TMA descriptors, split planning,
+// kernel launches.  Declarations and their contracts are in include/fa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fa_status fail(fa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // clear a sticky launch error
+  return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+// Per-device status word the kernels OR error bits into.
+__device__ uint32_t g_fa_status_word;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  uint32_t* status = nullptr;  // device address of g_fa_status_word
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+fa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    di.supported = (major == 10 && minor == 3);
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_fa_status_word)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    di.status = static_cast<uint32_t*>(addr);
+    di.ready = true;
+  }
+  if (!di.supported) return fail(FA_ERR_UNSUPPORTED, "device %d is not sm_103 (GB300)", dev);
+  *out = &di;
+  return FA_OK;
+}
+
+fa_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return FA_OK;
+}
+
+// 3-D view [rows, heads, d] of a row-major bf16 tensor; box = 64 columns x 1 head x box_rows rows,
+// 128-byte swizzle (the layout the kernels' shared-memory descriptors assume).
+fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows, int box_rows,
+                   const char* name) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(const void* q, const void* k, const void* v, void* o, const float* lse, int B, int Hq,
+                       int Hkv, int d, float scale) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID, "q, k, v and o must be non-null");
+  if (B <= 0 || Hq <= 0 || Hkv <= 0) return fail(FA_ERR_INVALID, "B, Hq, Hkv must be positive");
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(FA_ERR_INVALID, "scale must be finite and > 0");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(FA_ERR_INVALID, "q, k, v, o must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(FA_ERR_INVALID, "lse must be 4-byte aligned");
+  return FA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_last_error(void) { return g_last_error.c_str(); }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                 int Nk, int d, float scale, int causal, int window, const int* seqlens_q, const int* seqlens_k,
+                 fa_stream_t stream) {
+  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, d, scale);
+  if (st != FA_OK) return st;
+  if (Nq <= 0 || Nk <= 0) return fail(FA_ERR_INVALID, "Nq and Nk must be positive");
+  if ((long long)B * Nq >= (1LL << 31) || (long long)B * Nk >= (1LL << 31))
+    return fail(FA_ERR_INVALID, "B * N must be below 2^31 rows");
+  if ((long long)Nq + Nk + (window > 0 ? window : 0) >= (1LL << 30))
+    return fail(FA_ERR_INVALID, "sequence lengths too large");
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  if ((st = get_encoder()) != FA_OK) return st;
+  const int bm = fa::prefill_block_m();
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, q, d, Hq, (long long)B * Nq, bm, "q")) != FA_OK) return st;
+  if ((st = make_map(&tk, k, d, Hkv, (long long)B * Nk, 128, "k")) != FA_OK) return st;
+  if ((st = make_map(&tv, v, d, Hkv, (long long)B * Nk, 128, "v")) != FA_OK) return st;
+  fa::PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = p.cu_k = nullptr;
+  p.seqlens_q = seqlens_q;
+  p.seqlens_k = seqlens_k;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.group = Hq / Hkv;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.window = window > 0 ? window : 0;
+  p.err = di->status;
+  const int n_qtiles = (Nq + bm - 1) / bm;
+  if (n_qtiles > 65535 || B > 65535) return fail(FA_ERR_INVALID, "grid too large");
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, n_qtiles, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return FA_OK;
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                        int causal, int window, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                        const int* cu_seqlens_q_host, fa_stream_t stream) {
+  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, d, scale);
+  if (st != FA_OK) return st;
+  if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID, "cu_seqlens_q/k must be non-null");
+  if (total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(FA_ERR_INVALID, "totals and max lengths must be >= 0");
+  if ((long long)max_seqlen_q + max_seqlen_k + (window > 0 ? window : 0) >= (1LL << 30))
+    return fail(FA_ERR_INVALID, "sequence lengths too large");
+  if (cu_seqlens_q_host) {
+    if (cu_seqlens_q_host[0] != 0) return fail(FA_ERR_INVALID, "cu_seqlens_q[0] must be 0");
+    for (int b = 0; b < B; ++b) {
+      const int len = cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b];
+      if (len < 0) return fail(FA_ERR_INVALID, "cu_seqlens_q must be non-decreasing (at %d)", b);
+      if (len > max_seqlen_q) return fail(FA_ERR_INVALID, "sequence %d longer than max_seqlen_q", b);
+    }
+    if (cu_seqlens_q_host[B] != total_q) return fail(FA_ERR_INVALID, "cu_seqlens_q[B] != total_q");
+  }
+  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // nothing to compute
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  if ((st = get_encoder()) != FA_OK) return st;
+  const int bm = fa::prefill_block_m();
+  CUtensorMap tq, tk, tv;
+  const long long kr = total_k > 0 ? total_k : 1;  // a map needs one row; no key row is read when total_k = 0
+  if ((st = make_map(&tq, q, d, Hq, total_q, bm, "q")) != FA_OK) return st;
+  if ((st = make_map(&tk, k, d, Hkv, kr, 128, "k")) != FA_OK) return st;
+  if ((st = make_map(&tv, v, d, Hkv, kr, 128, "v")) != FA_OK) return st;
+  fa::PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.seqlens_q = p.seqlens_k = nullptr;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = max_seqlen_q;
+  p.Nk = max_seqlen_k;
+  p.group = Hq / Hkv;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.window = window > 0 ? window : 0;
+  p.err = di->status;
+  const int n_qtiles = (max_seqlen_q + bm - 1) / bm;
+  if (n_qtiles > 65535 || B > 65535) return fail(FA_ERR_INVALID, "grid too large");
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, n_qtiles, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill (varlen) launch");
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int d, int max_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || max_splits <= 0) return 0;
+  return (size_t)B * Hq * max_splits * ((size_t)d + 1) * sizeof(float);
+}
+
+namespace {
+
+struct DecodePlan {
+  int chunk;
+  int max_splits;
+};
+
+DecodePlan plan_decode(int B, int Hkv, int group, int Ncap, int window, const int* lens_host, int num_splits,
+                       int sm_count) {
+  const int bn = fa::decode_block_n();
+  const int cap = window > 0 ? (window < Ncap ? window : Ncap) : Ncap;
+  long long total = 0;
+  int longest = 0;
+  for (int b = 0; b < B; ++b) {
+    int len = lens_host ? lens_host[b] : Ncap;
+    len = len < 0 ? 0 : (len > Ncap ? Ncap : len);
+    const int eff = window > 0 && len > window ? window : len;
+    total += eff;
+    longest = eff > longest ? eff : longest;
+  }
+  if (!lens_host) longest = cap;
+  if (longest <= 0) longest = 1;
+  int chunk;
+  if (num_splits > 0) {
+    chunk = (longest + num_splits - 1) / num_splits;
+  } else {
+    // Aim for ~8 resident-CTA waves of equal-sized chunks so the tail wave is short.
+    const long long units = (long long)sm_count * 2 * 8;
+    const long long row_blocks = (long long)Hkv * ((group + 15) / 16);
+    const long long keys = total * row_blocks;
+    chunk = (int)((keys + units - 1) / units);
+    if (chunk < 256) chunk = 256;
+  }
+  chunk = ((chunk + bn - 1) / bn) * bn;
+  if (chunk < bn) chunk = bn;
+  DecodePlan pl;
+  pl.chunk = chunk;
+  pl.max_splits = (longest + chunk - 1) / chunk;
+  if (pl.max_splits < 1) pl.max_splits = 1;
+  return pl;
+}
+
+}  // namespace
+
+int fa_decode_max_splits(int B, int Hq, int Hkv, int Ncap, int window, const int* seqlens_k_host,
+                         int num_splits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Ncap <= 0 || Hq % Hkv != 0 || num_splits < 0) return 0;
+  int sm = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm <= 0) {
+    cudaGetLastError();
+    sm = 152;
+  }
+  return plan_decode(B, Hkv, Hq / Hkv, Ncap, window, seqlens_k_host, num_splits, sm).max_splits;
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                    int Hkv, int Ncap, int d, float scale, int window, const int* seqlens_k,
+                    const int* seqlens_k_host, int num_splits, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+  fa_status st = check_common(q, k_cache, v_cache, o, lse, B, Hq, Hkv, d, scale);
+  if (st != FA_OK) return st;
+  if (Ncap <= 0) return fail(FA_ERR_INVALID, "Ncap must be positive");
+  if (!seqlens_k) return fail(FA_ERR_INVALID, "seqlens_k must be non-null");
+  if (num_splits < 0) return fail(FA_ERR_INVALID, "num_splits must be >= 0");
+  if ((long long)B * Ncap >= (1LL << 31)) return fail(FA_ERR_INVALID, "B * Ncap must be below 2^31 rows");
+  if (B > 65535) return fail(FA_ERR_INVALID, "B too large");
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const DecodePlan pl = plan_decode(B, Hkv, Hq / Hkv, Ncap, window, seqlens_k_host, num_splits, di->sm_count);
+  const size_t need = fa_decode_workspace_size(B, Hq, d, pl.max_splits);
+  if (!workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
+  if (!aligned16(workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (pl.max_splits > 65535) return fail(FA_ERR_INVALID, "too many splits");
+  if ((st = get_encoder()) != FA_OK) return st;
+  CUtensorMap tk, tv;
+  const int bn = fa::decode_block_n();
+  if ((st = make_map(&tk, k_cache, d, Hkv, (long long)B * Ncap, bn, "k_cache")) != FA_OK) return st;
+  if ((st = make_map(&tv, v_cache, d, Hkv, (long long)B * Ncap, bn, "v_cache")) != FA_OK) return st;
+  fa::DecodeParams p{};
+  p.q = q;
+  p.o = o;
+  p.lse = lse;
+  p.seqlens_k = seqlens_k;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = p.o_part + (size_t)B * Hq * pl.max_splits * d;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Ncap = Ncap;
+  p.group = Hq / Hkv;
+  p.chunk = pl.chunk;
+  p.max_splits = pl.max_splits;
+  p.window = window > 0 ? window : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.err = di->status;
+  cudaError_t e = fa::launch_decode(d, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return FA_OK;
+}
+
+fa_status fa_device_status(uint32_t* bits, int clear) {
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t v = 0;
+  if ((e = cudaMemcpy(&v, di->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  if (clear && v) {
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpy(di->status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear status word");
+  }
+  if (bits) *bits = v;
+  if (v) return fail(FA_ERR_TIMEOUT, "device status word 0x%x (bit0 wait timeout, bit1 bounds)", v);
+  return FA_OK;
+}
+
+}  // extern "C"

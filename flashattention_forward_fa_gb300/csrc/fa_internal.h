@@ -1,0 +1,47 @@
+// Host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+struct PrefillParams {
+  void* o;                 // bf16 output
+  float* lse;              // fp32 LSE or nullptr
+  const int* cu_q;         // packed layout: int32 [B + 1] (nullptr otherwise)
+  const int* cu_k;
+  const int* seqlens_q;    // padded layout: int32 [B] valid lengths (nullptr = full)
+  const int* seqlens_k;
+  int B, Hq, Hkv, Nq, Nk;  // dense/padded: rows per sequence; packed: max lengths
+  int group;               // Hq / Hkv
+  float scale_log2;        // scale * log2(e)
+  int causal, window;
+  uint32_t* err;           // device status word
+};
+
+struct DecodeParams {
+  const void* q;           // bf16 [B, Hq, d]
+  void* o;                 // bf16 [B, Hq, d]
+  float* lse;              // fp32 [B, Hq] or nullptr
+  const int* seqlens_k;    // int32 [B]
+  float* o_part;           // fp32 [B, Hq, max_splits, d]
+  float* lse_part;         // fp32 [B, Hq, max_splits]
+  int B, Hq, Hkv, Ncap, group;
+  int chunk;               // keys per split (multiple of 64)
+  int max_splits;
+  int window;
+  float scale_log2;
+  uint32_t* err;
+};
+
+cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int n_qtiles, cudaStream_t stream);
+int prefill_block_m();
+
+cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                          cudaStream_t stream);
+int decode_block_n();
+
+}  // namespace fa

@@ -1,0 +1,155 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) attention-forward library (libfa_gb300.so).
+ *
+ * The library computes the fused attention forward
+ *     O = softmax(Q K^T * scale + mask) V,      LSE = log-sum-exp of each score row,
+ * with a running-max / running-sum (online) softmax, so the score matrix never
+ * reaches device memory.  The operation and its modes are those of the
+ * ops-transformer pages:
+ *   - the formula: jsqmd page "CANN Transformer算子库ops-transformer深度实践",
+ *     §二 "SelfAttention的基础实现与瓶颈";
+ *   - the fused, tiled evaluation (Q by row blocks, K/V by column blocks, all
+ *     blocks reduced on chip): same page, §二 "FlashAttention的融合计算思想", and
+ *     the hwcomputing.csdn.net page, §2.1 "分块计算策略与SRAM访存优化";
+ *   - the max-subtracted softmax kept in fp32 with bf16/fp16 matmul inputs:
+ *     hwcomputing.csdn.net page, §2.2 "数值稳定性优化";
+ *   - causal, sliding-window and MQA/GQA modes: jsqmd page, §一 "核心能力矩阵"
+ *     and §二 "因果掩码与解码优化" (implicit mask, no N x N mask tensor);
+ *   - per-sequence valid lengths with no compute on padding: agent.csdn.net BERT
+ *     walkthrough, 第三章 (actual_seq_q / actual_seq_kv) and 第六章;
+ *   - incremental decode (one new token against the cached K/V): agent.csdn.net
+ *     walkthrough, 结尾.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors live in device memory, are contiguous and row-major, and are
+ *     owned by the caller; the library allocates no device memory.
+ *   - q, k, v, o, caches: bf16.  lse and workspace: fp32.  Head dim d is 64 or 128.
+ *   - Hq % Hkv == 0; query head h reads KV head h / (Hq / Hkv) (contiguous groups).
+ *   - scale is the multiplier applied to Q K^T (e.g. 1/sqrt(d)); it must be > 0.
+ *   - causal: bottom-right aligned — row i of a sequence with Lq queries and Lk
+ *     keys may see key j iff j <= i + Lk - Lq.
+ *   - window > 0: with causal, also j > i + Lk - Lq - window (the window holds the
+ *     diagonal, so window = 1 keeps only it); without causal, |i + Lk - Lq - j| < window.
+ *     window <= 0: no window.
+ *   - A row that sees no key gets O = 0 and LSE = -inf.
+ *   - LSE is the natural log of the row's normaliser in scaled-score units.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Errors
+ *     found on the host return before any launch; a failed launch returns
+ *     FA_ERR_CUDA.  fa_last_error() describes the last failure of the calling
+ *     thread.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,     /* bad argument (null pointer, size, layout) */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not supported (d not 64/128, device not sm_103) */
+  FA_ERR_CUDA = 3,        /* CUDA runtime/driver error */
+  FA_ERR_TIMEOUT = 4      /* a kernel wait passed its time limit (see fa_device_status) */
+} fa_status;
+
+/*
+ * Prefill / encoder attention forward on the padded-batch layout.
+ *   q, o : [B, Nq, Hq, d] bf16          k, v : [B, Nk, Hkv, d] bf16
+ *   lse  : [B, Hq, Nq] fp32 (may be NULL)
+ *   seqlens_q, seqlens_k : NULL for full length, or device int32 [B] holding the
+ *       valid length of each sequence (values clamped to [0, Nq] / [0, Nk]); rows
+ *       and keys past a sequence's valid length take no part in the computation
+ *       (the pages' actual_seq_q / actual_seq_kv), and output rows i with
+ *       seqlens_q[b] <= i < Nq are written as O = 0, LSE = -inf.
+ * Returns FA_ERR_INVALID for null q/k/v/o, non-positive sizes, Hq % Hkv != 0,
+ * scale <= 0; FA_ERR_UNSUPPORTED for d not in {64, 128}.
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                 int causal, int window,
+                 const int* seqlens_q, const int* seqlens_k,
+                 fa_stream_t stream);
+
+/*
+ * Prefill on the packed variable-length layout (no padding rows at all).
+ *   q, o : [total_q, Hq, d] bf16        k, v : [total_k, Hkv, d] bf16
+ *   lse  : [Hq, total_q] fp32 (may be NULL)
+ *   cu_seqlens_q, cu_seqlens_k : device int32 [B + 1], non-decreasing,
+ *       cu[0] = 0, cu[B] = total; sequence b owns rows cu[b] .. cu[b+1]-1.
+ *   max_seqlen_q / max_seqlen_k : upper bounds of the per-sequence lengths
+ *       (the grid is sized from max_seqlen_q; longer sequences are an error the
+ *       host cannot see, so the caller must pass true bounds).
+ *   cu_seqlens_q_host : optional host copy of cu_seqlens_q; when given it is
+ *       checked (monotone, cu[0] = 0, cu[B] = total_q, lengths <= max_seqlen_q).
+ */
+FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int total_q, int total_k,
+                        int max_seqlen_q, int max_seqlen_k, int d, float scale,
+                        int causal, int window,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k,
+                        const int* cu_seqlens_q_host,
+                        fa_stream_t stream);
+
+/*
+ * Bytes of fp32 workspace fa_decode needs for a given split bound
+ * (partial outputs [B, Hq, max_splits, d] and partial LSE [B, Hq, max_splits]).
+ */
+FA_API size_t fa_decode_workspace_size(int B, int Hq, int d, int max_splits);
+
+/*
+ * Single-query incremental decode over a KV cache, split over the key axis
+ * and merged by a log-sum-exp combine kernel.
+ *   q, o : [B, Hq, d] bf16 (the one new token of each sequence)
+ *   k_cache, v_cache : [B, Ncap, Hkv, d] bf16; sequence b's keys are slots
+ *       0 .. seqlens_k[b]-1 (the new token's K/V already appended)
+ *   lse : [B, Hq] fp32 (may be NULL)
+ *   seqlens_k : device int32 [B], values clamped to [0, Ncap]
+ *   seqlens_k_host : optional host copy used only to plan the split size
+ *   window : > 0 restricts the query to the last `window` keys
+ *   num_splits : 0 = choose automatically; otherwise the maximum number of
+ *       key chunks per sequence (each chunk a multiple of 64 keys)
+ *   workspace : device memory of at least fa_decode_workspace_size(B, Hq, d, S)
+ *       bytes, S the split bound actually used (fa_decode_max_splits tells it)
+ * Returns FA_ERR_INVALID when workspace is NULL or too small.
+ */
+FA_API fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    int B, int Hq, int Hkv, int Ncap, int d, float scale, int window,
+                    const int* seqlens_k, const int* seqlens_k_host,
+                    int num_splits, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/*
+ * The split bound S that fa_decode uses for the same arguments on the current
+ * device (size the workspace with fa_decode_workspace_size(B, Hq, d, S)).
+ * Returns 0 for invalid sizes.
+ */
+FA_API int fa_decode_max_splits(int B, int Hq, int Hkv, int Ncap, int window, const int* seqlens_k_host, int num_splits);
+
+/* Description of the calling thread's last error ("" if none). */
+FA_API const char* fa_last_error(void);
+
+/*
+ * Read (and optionally clear) the device status word of the current device:
+ * bit 0 = some kernel wait passed its time limit, bit 1 = a device-side bounds
+ * check fired.  Synchronises the device.  Returns FA_ERR_TIMEOUT when bits
+ * are set, FA_OK otherwise.
+ */
+FA_API fa_status fa_device_status(uint32_t* bits, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

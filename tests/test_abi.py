@@ -1,0 +1,142 @@
+"""CPU-side checks of the C ABI: the library builds/loads, exports every symbol
+declared in include/fa.h, and rejects bad arguments on the host before any
+CUDA call.  No compute runs here (there is no GPU)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from flashattention_forward_fa_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    for name in ("fa_fwd", "fa_fwd_varlen", "fa_decode", "fa_decode_workspace_size", "fa_decode_max_splits",
+                 "fa_last_error", "fa_device_status"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from flashattention_forward_fa_gb300 import build
+    out = subprocess.check_output(["nm", "-D", "--defined-only", build.LIB]).decode()
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    for name in declared_symbols():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_no_cpu_fallback_symbols(lib):
+    # the product library carries no host implementation of the attention math:
+    # every compute entry point launches kernels, nothing links the oracle
+    from flashattention_forward_fa_gb300 import build
+    out = subprocess.check_output(["nm", "-D", build.LIB]).decode()
+    assert "oracle" not in out
+
+
+def _binding():
+    import flashattention_forward_fa_gb300 as fa
+    from flashattention_forward_fa_gb300 import _binding as b
+    b.load_library()
+    return fa, b
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    _, b = _binding()
+    L = b.load_library()
+    dummy = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+    # null q
+    assert L.fa_fwd(None, dummy, dummy, dummy, None, 1, 2, 2, 8, 8, 64, 0.125, 0, 0, None, None, None) == 1
+    assert b"non-null" in L.fa_last_error()
+    # Hq % Hkv != 0
+    assert L.fa_fwd(dummy, dummy, dummy, dummy, None, 1, 6, 4, 8, 8, 64, 0.125, 0, 0, None, None, None) == 1
+    assert b"multiple" in L.fa_last_error()
+    # unsupported head dim
+    assert L.fa_fwd(dummy, dummy, dummy, dummy, None, 1, 2, 2, 8, 8, 96, 0.125, 0, 0, None, None, None) == 2
+    # scale <= 0
+    assert L.fa_fwd(dummy, dummy, dummy, dummy, None, 1, 2, 2, 8, 8, 64, 0.0, 0, 0, None, None, None) == 1
+    # non-positive sizes
+    assert L.fa_fwd(dummy, dummy, dummy, dummy, None, 0, 2, 2, 8, 8, 64, 0.1, 0, 0, None, None, None) == 1
+    assert L.fa_fwd(dummy, dummy, dummy, dummy, None, 1, 2, 2, 0, 8, 64, 0.1, 0, 0, None, None, None) == 1
+    # misaligned pointer
+    odd = ctypes.c_void_p(0x1002)
+    assert L.fa_fwd(odd, dummy, dummy, dummy, None, 1, 2, 2, 8, 8, 64, 0.1, 0, 0, None, None, None) == 1
+    assert b"aligned" in L.fa_last_error()
+
+
+def test_varlen_host_cu_seqlens_checked(lib):
+    _, b = _binding()
+    L = b.load_library()
+    dummy = ctypes.c_void_p(0x1000)
+    IntArr = ctypes.c_int * 4
+    bad_start = IntArr(1, 3, 5, 8)
+    assert L.fa_fwd_varlen(dummy, dummy, dummy, dummy, None, 3, 2, 2, 8, 8, 8, 8, 64, 0.1, 0, 0, dummy, dummy,
+                           ctypes.cast(bad_start, b._ip), None) == 1
+    non_mono = IntArr(0, 5, 3, 8)
+    assert L.fa_fwd_varlen(dummy, dummy, dummy, dummy, None, 3, 2, 2, 8, 8, 8, 8, 64, 0.1, 0, 0, dummy, dummy,
+                           ctypes.cast(non_mono, b._ip), None) == 1
+    assert b"non-decreasing" in L.fa_last_error()
+    wrong_total = IntArr(0, 3, 5, 7)
+    assert L.fa_fwd_varlen(dummy, dummy, dummy, dummy, None, 3, 2, 2, 8, 8, 8, 8, 64, 0.1, 0, 0, dummy, dummy,
+                           ctypes.cast(wrong_total, b._ip), None) == 1
+    too_long = IntArr(0, 6, 7, 8)
+    assert L.fa_fwd_varlen(dummy, dummy, dummy, dummy, None, 3, 2, 2, 8, 8, 4, 8, 64, 0.1, 0, 0, dummy, dummy,
+                           ctypes.cast(too_long, b._ip), None) == 1
+    # null cu_seqlens
+    assert L.fa_fwd_varlen(dummy, dummy, dummy, dummy, None, 3, 2, 2, 8, 8, 8, 8, 64, 0.1, 0, 0, None, dummy,
+                           None, None) == 1
+
+
+def test_decode_arguments_checked(lib):
+    _, b = _binding()
+    L = b.load_library()
+    dummy = ctypes.c_void_p(0x1000)
+    # null seqlens
+    assert L.fa_decode(dummy, dummy, dummy, dummy, None, 2, 8, 2, 64, 128, 0.1, 0, None, None, 0, dummy, 1 << 20,
+                       None) == 1
+    # negative num_splits
+    assert L.fa_decode(dummy, dummy, dummy, dummy, None, 2, 8, 2, 64, 128, 0.1, 0, dummy, None, -1, dummy,
+                       1 << 20, None) == 1
+
+
+def test_workspace_size_formula(lib):
+    _, b = _binding()
+    L = b.load_library()
+    assert L.fa_decode_workspace_size(64, 32, 128, 9) == 64 * 32 * 9 * 129 * 4
+    assert L.fa_decode_workspace_size(0, 32, 128, 9) == 0
+
+
+def test_decode_split_plan_bounds(lib):
+    _, b = _binding()
+    L = b.load_library()
+    # explicit split count: chunk = ceil(longest / n) rounded up to 64
+    lens = (ctypes.c_int * 3)(100, 1000, 640)
+    assert L.fa_decode_max_splits(3, 8, 2, 1024, 0, ctypes.cast(lens, b._ip), 4) == 4
+    # one split when asked for one
+    assert L.fa_decode_max_splits(3, 8, 2, 1024, 0, ctypes.cast(lens, b._ip), 1) == 1
+    # window caps the key range
+    assert L.fa_decode_max_splits(3, 8, 2, 1024, 64, None, 8) == 1
+    assert L.fa_decode_max_splits(0, 8, 2, 1024, 0, None, 0) == 0
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    fa, b = _binding()
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(b.FAError):
+        fa.fa_fwd(q, q, q)

@@ -1,0 +1,105 @@
+"""GPU parity of the split-KV decode path (split kernel + combine) against the
+fp64 oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+from fa_workloads import DECODE_CACHE, DecodeCase, make_decode, shrink
+from tests._util import check, gpu_decode, oracle_decode_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _all_pairs(B, Hq):
+    return np.array([(b, h) for b in range(B) for h in range(Hq)], dtype=np.int32)
+
+
+def _parity(case: DecodeCase, num_splits=0, with_host_lens=True, rows=None):
+    import flashattention_forward_fa_gb300 as fa
+    x = make_decode(case)
+    o, lse = gpu_decode(x, num_splits=num_splits, with_host_lens=with_host_lens)
+    rows = _all_pairs(case.B, case.Hq) if rows is None else rows
+    go = o.float().cpu().numpy()[rows[:, 0], rows[:, 1]].astype(np.float64)
+    gl = lse.cpu().numpy()[rows[:, 0], rows[:, 1]].astype(np.float64)
+    ro, rl = oracle_decode_rows(x, rows)
+    res = check(go, gl, ro, rl, case.name)
+    assert fa.fa_device_status() == 0
+    return x, o, lse, res
+
+
+def test_decode_cache_full_size_sampled():
+    # B=64, Hq=32, Hkv=8, d=128, cache 8192, lengths uniform in [512, 8192]
+    rng = np.random.default_rng(5)
+    bs = sorted(set([0, 63] + rng.integers(0, 64, 14).tolist()))
+    rows = np.array([(b, h) for b in bs for h in range(32)], dtype=np.int32)
+    _parity(DECODE_CACHE, rows=rows)
+
+
+def test_decode_cache_reduced_full():
+    _parity(shrink(DECODE_CACHE, name="decode_small", B=8, Ncap=2048, len_range=(1, 2048)))
+
+
+@pytest.mark.parametrize("case", [
+    DecodeCase("mha_d64", B=3, Hq=4, Hkv=4, Ncap=500, d=64, lens=[1, 63, 500], seed=41),
+    DecodeCase("gqa8_d128", B=4, Hq=16, Hkv=2, Ncap=1000, d=128, lens=[64, 65, 999, 1000], seed=42),
+    DecodeCase("mqa_g32", B=2, Hq=32, Hkv=1, Ncap=700, d=128, lens=[700, 129], seed=43),
+    DecodeCase("g16_d64", B=2, Hq=16, Hkv=1, Ncap=300, d=64, lens=[257, 3], seed=44),
+    DecodeCase("g3_odd", B=2, Hq=6, Hkv=2, Ncap=333, d=128, lens=[333, 200], seed=45),
+    DecodeCase("empty_seq", B=3, Hq=8, Hkv=2, Ncap=256, d=128, lens=[0, 256, 1], seed=46),
+    DecodeCase("window", B=3, Hq=8, Hkv=2, Ncap=1500, d=128, lens=[1500, 100, 700], window=256, seed=47),
+    DecodeCase("window1", B=2, Hq=4, Hkv=1, Ncap=200, d=64, lens=[200, 5], window=1, seed=48),
+], ids=lambda c: c.name)
+def test_decode_edges(case):
+    _parity(case)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 5, 8, 16, 33])
+def test_every_split_count(num_splits):
+    _parity(DecodeCase("splits", B=3, Hq=8, Hkv=2, Ncap=2100, d=128, lens=[2100, 1, 777], seed=49),
+            num_splits=num_splits)
+
+
+def test_split_count_invariance():
+    # changing the split count only changes fp32 summation order
+    case = DecodeCase("inv", B=4, Hq=8, Hkv=2, Ncap=4096, d=128, len_range=(1, 4096), seed=50)
+    x = make_decode(case)
+    outs = [gpu_decode(x, num_splits=s) for s in (1, 4, 16)]
+    for o, l in outs[1:]:
+        assert (o.float() - outs[0][0].float()).abs().max().item() <= 1e-2
+        assert (l - outs[0][1]).abs().max().item() <= 1e-3
+
+
+def test_without_host_lengths_matches():
+    case = DecodeCase("nohost", B=4, Hq=8, Hkv=2, Ncap=3000, d=128, len_range=(1, 3000), seed=51)
+    _parity(case, with_host_lens=False)
+
+
+def test_garbage_past_length_is_ignored():
+    # cache slots past each sequence's length hold NaN/Inf: they must not leak into the output
+    import flashattention_forward_fa_gb300 as fa
+    case = DecodeCase("nan_tail", B=3, Hq=8, Hkv=2, Ncap=400, d=128, lens=[1, 130, 333], seed=52)
+    x = make_decode(case)
+    k = x.k_cache.clone()
+    v = x.v_cache.clone()
+    for b, n in enumerate(x.lens):
+        k[b, n:] = float("nan")
+        v[b, n:] = float("inf")
+    lens = torch.tensor(x.lens, dtype=torch.int32, device="cuda")
+    o, lse = fa.fa_decode(x.q.cuda(), k.cuda(), v.cuda(), lens, seqlens_k_host=x.lens)
+    torch.cuda.synchronize()
+    ref_o, ref_l = gpu_decode(x)
+    assert torch.isfinite(o.float()).all()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+
+
+def test_decode_matches_prefill_last_row():
+    # a decode step equals the last row of a causal prefill over the same keys
+    import flashattention_forward_fa_gb300 as fa
+    case = DecodeCase("vs_prefill", B=2, Hq=8, Hkv=2, Ncap=640, d=128, lens=[640, 640], seed=53)
+    x = make_decode(case)
+    o, lse = gpu_decode(x)
+    q4 = x.q.reshape(2, 1, 8, 128).cuda()
+    po, pl = fa.fa_fwd(q4, x.k_cache.cuda(), x.v_cache.cuda(), causal=True)
+    assert (po[:, 0].float() - o.float()).abs().max().item() <= 1e-2
+    assert (pl[:, :, 0] - lse).abs().max().item() <= 1e-3
