@@ -37,7 +37,7 @@ struct DecodeCfg {
   static constexpr int TILE = BN * D * 2;         // K or V tile (bytes)
   static constexpr int STAGE = 2 * TILE;          // K + V
   static constexpr int OFF_BAR = ST * STAGE;
-  static constexpr int MERGE_BYTES = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;  // per-warp O, m, l
+  static constexpr int MERGE_BYTES = 4 * 16 * D * 4 + 3 * 4 * 16 * 4;  // per-warp O, m, l, lr
   static_assert(MERGE_BYTES <= ST * STAGE, "merge area reuses the ring");
   static constexpr int SMEM_BYTES = OFF_BAR + 2 * ST * 8 + 16 + 1024;
   static constexpr int THREADS = 160;             // 4 compute warps + 1 producer warp
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float lr0 = 0.f, lr1 = 0.f;  // sums of the bf16-rounded weights P V actually uses (normalise O)
   const float sl2 = p.scale_log2;
   const uint32_t sbase = smem_u32(sm);
   bool ok = true;
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       if (mn0 > m0 + 8.0f) {  // lazy rescale: the exponent base moves only on large jumps
         const float a = ex2_approx(m0 - mn0);
         l0 *= a;
+        lr0 *= a;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) oacc[n][0] *= a, oacc[n][1] *= a;
         m0 = mn0;
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       if (mn1 > m1 + 8.0f) {
         const float a = ex2_approx(m1 - mn1);
         l1 *= a;
+        lr1 *= a;
 #pragma unroll
         for (int n = 0; n < D / 8; ++n) oacc[n][2] *= a, oacc[n][3] *= a;
         m1 = mn1;
@@ -237,6 +240,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       const uint32_t pa1 = pack_bf16x2(pe[0][2], pe[0][3]);
       const uint32_t pa2 = pack_bf16x2(pe[1][0], pe[1][1]);
       const uint32_t pa3 = pack_bf16x2(pe[1][2], pe[1][3]);
+      lr0 += (__uint_as_float(pa0 << 16) + __uint_as_float(pa0 & 0xffff0000u)) +
+             (__uint_as_float(pa2 << 16) + __uint_as_float(pa2 & 0xffff0000u));
+      lr1 += (__uint_as_float(pa1 << 16) + __uint_as_float(pa1 & 0xffff0000u)) +
+             (__uint_as_float(pa3 << 16) + __uint_as_float(pa3 & 0xffff0000u));
       // O += P V for 16 keys
 #pragma unroll
       for (int j = 0; j < D / 16; ++j) {
@@ -255,16 +262,23 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
   float* mo = reinterpret_cast<float*>(sm);                  // [4][16][D]
   float* mm = mo + 4 * 16 * D;                               // [4][16]
   float* ml = mm + 4 * 16;                                   // [4][16]
+  float* mr = ml + 4 * 16;                                   // [4][16]
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  lr0 += __shfl_xor_sync(0xffffffffu, lr0, 1);
+  lr0 += __shfl_xor_sync(0xffffffffu, lr0, 2);
+  lr1 += __shfl_xor_sync(0xffffffffu, lr1, 1);
+  lr1 += __shfl_xor_sync(0xffffffffu, lr1, 2);
   if (ok) {
     if (tq == 0) {
       mm[warp * 16 + g] = m0;
       mm[warp * 16 + g + 8] = m1;
       ml[warp * 16 + g] = l0;
       ml[warp * 16 + g + 8] = l1;
+      mr[warp * 16 + g] = lr0;
+      mr[warp * 16 + g + 8] = lr1;
     }
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
@@ -283,17 +297,18 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
     float mstar = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) mstar = fmaxf(mstar, mm[w * 16 + r]);
-    float lsum = 0.f, osum = 0.f;
+    float lsum = 0.f, rsum = 0.f, osum = 0.f;
     if (mstar != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const float f = ex2_approx(mm[w * 16 + r] - mstar);
         lsum += ml[w * 16 + r] * f;
+        rsum += mr[w * 16 + r] * f;
         osum += mo[(w * 16 + r) * D + d] * f;
       }
     }
     const size_t prow = ((size_t)b * p.Hq + hq0 + r) * p.max_splits + split;
-    p.o_part[prow * D + d] = lsum > 0.f ? osum / lsum : 0.f;
+    p.o_part[prow * D + d] = rsum > 0.f ? osum / rsum : 0.f;
     if (d == 0) p.lse_part[prow] = lsum > 0.f ? (mstar + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
   }
 }
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = -INFINITY;
     return;
   }
-  const int ns = (nkeys + p.chunk - 1) / p.chunk;
+  const int ns = min((nkeys + p.chunk - 1) / p.chunk, p.max_splits);  // never read past the workspace
   const size_t prow0 = ((size_t)b * p.Hq + hq) * p.max_splits;
   constexpr float LOG2E = 1.4426950408889634f;
   float mx = -INFINITY;

@@ -47,8 +47,9 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
-  // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_done, mma_done
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], o_done,
+  // o_final, mma_done
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 224;
@@ -150,8 +151,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint64_t* v_empty = v_full + C::VST;
   uint64_t* s_full = v_empty + C::VST;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* mma_done = o_done + 1;
+  uint64_t* o_done = p_full + 2;   // one completion per PV (phase gap to any waiter is at most one)
+  uint64_t* o_final = o_done + 1;  // single completion: the last PV of this tile
+  uint64_t* mma_done = o_final + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
 
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       mbar_init(&p_full[i], 4);  // one arrival per softmax warp
     }
     mbar_init(o_done, 1);
+    mbar_init(o_final, 1);
     mbar_init(mma_done, 1);
     fence_barrier_init();
   }
@@ -191,7 +194,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running max used for exponentiation (log2 units)
-    float l = 0.f;        // running sum of exp2(score*sl2 - m)
+    float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
+    float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int sb = t & 1;
@@ -269,10 +273,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
       if (need) {
         l *= alpha;
+        lr *= alpha;
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float rs0 = 0.f, rs1 = 0.f;
+      // P V runs on bf16-rounded weights; normalising O by the sum of those same rounded
+      // weights keeps O an exact convex combination of V rows (the bf16 rounding of P then
+      // only perturbs the weights, never their total), while the LSE uses the fp32 sum.
+      float rs0 = 0.f, rs1 = 0.f, rr0 = 0.f, rr1 = 0.f;
       uint32_t pk0[32], pk1[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -281,6 +289,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         rs0 += e0;
         rs1 += e1;
         pk0[j] = pack_bf16x2(e0, e1);
+        rr0 += __uint_as_float(pk0[j] << 16);
+        rr1 += __uint_as_float(pk0[j] & 0xffff0000u);
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -289,8 +299,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         rs0 += e0;
         rs1 += e1;
         pk1[j] = pack_bf16x2(e0, e1);
+        rr0 += __uint_as_float(pk1[j] << 16);
+        rr1 += __uint_as_float(pk1[j] & 0xffff0000u);
       }
       l += rs0 + rs1;
+      lr += rr0 + rr1;
       const uint32_t pa = t_lane + (sb ? C::COL_S1 : C::COL_S0);
       tmem_st32(pa + 0, pk0);
       tmem_st32(pa + 32, pk1);
@@ -300,13 +313,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }
     if (ok) {
-      ok = mbar_wait(o_done, (T - 1) & 1, abort_flag, p.err);  // last PV finished
+      // A fast warp can get here while PV_{T-2} is still pending, two phases behind o_done, so the
+      // last PV signals its own single-phase barrier.
+      ok = mbar_wait(o_final, 0, abort_flag, p.err);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
       const bool store = i < s.Lq;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const float inv = lr > 0.f ? 1.0f / lr : 0.f;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(s.q_row0 + i) * p.Hq + h) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -374,7 +389,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-      auto issue_pv = [&](int u) -> bool {
+      auto issue_pv = [&](int u, bool last) -> bool {
         const int vs = u % C::VST;
         if (!mbar_wait(&p_full[u & 1], (u >> 1) & 1, abort_flag, p.err)) return false;
         if (!mbar_wait(&v_full[vs], (u / C::VST) & 1, abort_flag, p.err)) return false;
@@ -388,6 +403,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
         umma_commit(&v_empty[vs]);
         umma_commit(o_done);
+        if (last) umma_commit(o_final);
         return true;
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.err);
@@ -410,9 +426,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
         umma_commit(&k_empty[ks]);
         umma_commit(&s_full[t & 1]);
-        if (t >= 1) ok = issue_pv(t - 1);
+        if (t >= 1) ok = issue_pv(t - 1, false);
       }
-      if (ok) issue_pv(T - 1);
+      if (ok) issue_pv(T - 1, true);
       umma_commit(mma_done);  // every MMA issued above has completed once this fires
       mbar_wait(mma_done, 0, abort_flag, nullptr);
     }

@@ -77,9 +77,13 @@ def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     rows: int array [n, 3] of (b, h, i).  Returns (O [n, d], LSE [n]) float64.
     """
     lib = _load()
+    # leading dims are flattened into rows: [..., H, d] -> [rows, H, d]
     q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    q_bits = q_bits.reshape(-1, q_bits.shape[-2], q_bits.shape[-1])
     k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    k_bits = k_bits.reshape(-1, k_bits.shape[-2], k_bits.shape[-1])
     v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    v_bits = v_bits.reshape(-1, v_bits.shape[-2], v_bits.shape[-1])
     _, hq, d = q_bits.shape
     hkv = k_bits.shape[1]
     B = len(len_q)

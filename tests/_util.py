@@ -4,6 +4,14 @@ the same bf16 inputs, and compare with the acceptance tolerances.
 Tolerances (fixed by the acceptance criteria, not tuned): bf16 O max-abs error
 <= 1e-2 and relative RMS <= 5e-3; fp32 LSE max-abs error <= 1e-3 where finite;
 -inf LSE must match -inf exactly and such rows must be exactly 0.
+
+The named workloads are checked with exactly those numbers (``strict=True``).
+Synthetic edge cases with deliberately sharpened scores can produce outputs
+|O| > 1.28, where the bf16 output format by itself cannot honour 1e-2: the
+round-to-nearest of the stored value alone errs by up to 2^-8 |O| (half an
+ulp of an 8-significant-bit format), and rounding the weights P to bf16 adds
+at most as much again.  For those cases (``strict=False``) element i may err by
+max(1e-2, 2^-7 |O_i|) — identical to 1e-2 wherever |O_i| <= 1.28.
 """
 
 from __future__ import annotations
@@ -82,7 +90,8 @@ def sample_rows(x: PrefillInputs, per_head: int, heads=None, seed=0) -> np.ndarr
     return np.asarray(out, dtype=np.int32).reshape(-1, 3)
 
 
-def check(o_gpu: np.ndarray, l_gpu: np.ndarray, o_ref: np.ndarray, l_ref: np.ndarray, what: str = ""):
+def check(o_gpu: np.ndarray, l_gpu: np.ndarray, o_ref: np.ndarray, l_ref: np.ndarray, what: str = "",
+          strict: bool = True):
     """Assert the acceptance tolerances; return a dict of the measured errors."""
     assert o_gpu.shape == o_ref.shape, (o_gpu.shape, o_ref.shape)
     empty_ref = np.isneginf(l_ref)
@@ -99,7 +108,13 @@ def check(o_gpu: np.ndarray, l_gpu: np.ndarray, o_ref: np.ndarray, l_ref: np.nda
         rel_rms = math.sqrt(float(np.sum(d ** 2)) / denom) if denom > 0 else 0.0
         lse_err = float(np.abs(l_gpu[fin] - l_ref[fin]).max())
         res.update(o_max_abs=max_abs, o_rel_rms=rel_rms, lse_max_abs=lse_err)
-        assert max_abs <= O_MAX_ABS, f"{what}: O max-abs {max_abs:.3e} > {O_MAX_ABS}"
+        if strict:
+            assert max_abs <= O_MAX_ABS, f"{what}: O max-abs {max_abs:.3e} > {O_MAX_ABS}"
+        else:
+            bound = np.maximum(O_MAX_ABS, np.abs(o_ref[fin]) * 2.0 ** -7)
+            worst = float((np.abs(d) / bound).max())
+            res["o_bound_ratio"] = worst
+            assert worst <= 1.0, f"{what}: O error exceeds max(1e-2, 2^-7|O|) by x{worst:.3f} (max-abs {max_abs:.3e})"
         assert rel_rms <= O_REL_RMS, f"{what}: O rel-RMS {rel_rms:.3e} > {O_REL_RMS}"
         assert lse_err <= LSE_MAX_ABS, f"{what}: LSE max-abs {lse_err:.3e} > {LSE_MAX_ABS}"
     return res
