@@ -28,6 +28,7 @@ _SIGS = {
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp, _sz, _vp]),
     "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _ip, _i]),
+    "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
 }
@@ -187,6 +188,32 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
                          int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(q)))
+    return o, lse
+
+
+def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens_k: torch.Tensor,
+                      window: int = 0, scale: Optional[float] = None, num_splits: int = 0, seqlens_k_host=None,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """fa_decode whose split partials use the library's fixed per-device scratch (no workspace).
+
+    For callers that cannot allocate device memory; pass ``out``/``lse`` to allocate nothing here
+    either.  Calls on one device share the scratch: do not let two of them overlap on the GPU."""
+    lib = load_library()
+    _need(q, "q")
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    _need(seqlens_k, "seqlens_k", torch.int32)
+    B, Hq, d = q.shape
+    _, Ncap, Hkv, _ = k_cache.shape
+    host = _host_ints(seqlens_k_host)
+    o = out if out is not None else torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    _check(lib.fa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d,
+                                 sc, int(window), _ptr(seqlens_k), ctypes.cast(host, _ip) if host is not None else None,
+                                 int(num_splits), _stream(q)))
     return o, lse
 
 

@@ -348,3 +348,65 @@ fa_status fa_device_status(uint32_t* bits, int clear) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Decode without any device allocation (fa_decode_noalloc, declared in include/fa.h).
+//
+// Some callers cannot call cudaMalloc: a plugin inside an inference engine that is handed only
+// its input and output buffers, or a serving loop that must never take the allocator's locks or
+// the device synchronisation an allocation can cause.  For them the split-KV partials live in
+// this fixed, file-scope device array instead of a caller workspace.  Every GPU that loads the
+// library holds the array until the process exits, so it is kept modest: 16 MiB, enough for the
+// partials of B x Hq x splits x (d + 1) fp32 values up to that size (for example B = 64, Hq = 32,
+// d = 128 with up to 15 splits).
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch, looked up once per device with that device current.
+void* g_scratch_addr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+fa_status decode_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    if (!p) return fail(FA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch) returned null");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                       int B, int Hq, int Hkv, int Ncap, int d, float scale, int window,
+                                       const int* seqlens_k, const int* seqlens_k_host, int num_splits,
+                                       fa_stream_t stream) {
+  // Reject problems whose partials do not fit before touching the device.
+  const int S = fa_decode_max_splits(B, Hq, Hkv, Ncap, window, seqlens_k_host, num_splits);
+  if (S > 0) {
+    const size_t need = fa_decode_workspace_size(B, Hq, d, S);
+    if (need > kNoAllocScratchBytes)
+      return fail(FA_ERR_INVALID,
+                  "fa_decode_noalloc: these sizes need %zu bytes of split scratch (B=%d, Hq=%d, d=%d, %d splits) "
+                  "but the built-in scratch holds %zu bytes; pass a smaller num_splits or call fa_decode "
+                  "with a caller-owned workspace",
+                  need, B, Hq, d, S, kNoAllocScratchBytes);
+  }
+  void* scratch = nullptr;
+  fa_status st = decode_scratch_address(&scratch);
+  if (st != FA_OK) return st;
+  return fa_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Ncap, d, scale, window, seqlens_k, seqlens_k_host,
+                   num_splits, scratch, kNoAllocScratchBytes, stream);
+}
+

@@ -137,6 +137,35 @@ FA_API fa_status fa_decode(const void* q, const void* k_cache, const void* v_cac
  */
 FA_API int fa_decode_max_splits(int B, int Hq, int Hkv, int Ncap, int window, const int* seqlens_k_host, int num_splits);
 
+/*
+ * fa_decode without any device allocation.  The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc — for example a
+ * plugin inside an inference engine that is handed only its input and output
+ * buffers, or a serving loop that must not take the allocator's locks or the
+ * device synchronisation an allocation can cause.
+ *
+ * Arguments and results are those of fa_decode, minus the workspace: the split
+ * partials go to a fixed scratch array inside the library: 16 MiB (16777216
+ * bytes) per device, held by every GPU that loads the library until the
+ * process exits — enough for B = 64, Hq = 32, d = 128 with up to 15 splits.
+ * A problem whose partials
+ * (fa_decode_workspace_size for the split bound fa_decode_max_splits gives)
+ * exceed it is rejected with FA_ERR_INVALID before any launch; a smaller
+ * num_splits lowers the need.  The function calls no allocator: not cudaMalloc,
+ * cudaFree, nor any allocating library routine.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress with that device current) and caches it; make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array, which keeps the last call's contents (nothing in it needs to start at
+ * zero): calls that can overlap on the GPU — on different streams without
+ * ordering between them — race on it and must not be issued that way.
+ */
+FA_API fa_status fa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                   int B, int Hq, int Hkv, int Ncap, int d, float scale, int window,
+                                   const int* seqlens_k, const int* seqlens_k_host, int num_splits,
+                                   fa_stream_t stream);
+
 /* Description of the calling thread's last error ("" if none). */
 FA_API const char* fa_last_error(void);
 
