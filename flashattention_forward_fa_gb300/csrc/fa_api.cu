@@ -139,7 +139,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   if ((st = get_encoder()) != FA_OK) return st;
-  const int bm = fa::prefill_block_m();
+  const int bm = fa::prefill_box_rows();
   CUtensorMap tq, tk, tv;
   if ((st = make_map(&tq, q, d, Hq, (long long)B * Nq, bm, "q")) != FA_OK) return st;
   if ((st = make_map(&tk, k, d, Hkv, (long long)B * Nk, 128, "k")) != FA_OK) return st;
@@ -160,9 +160,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.causal = causal ? 1 : 0;
   p.window = window > 0 ? window : 0;
   p.err = di->status;
-  const int n_qtiles = (Nq + bm - 1) / bm;
-  if (n_qtiles > 65535 || B > 65535) return fail(FA_ERR_INVALID, "grid too large");
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, n_qtiles, reinterpret_cast<cudaStream_t>(stream));
+  if (B > 65535) return fail(FA_ERR_INVALID, "grid too large");
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, Nq, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }
@@ -191,7 +190,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   if ((st = get_encoder()) != FA_OK) return st;
-  const int bm = fa::prefill_block_m();
+  const int bm = fa::prefill_box_rows();
   CUtensorMap tq, tk, tv;
   const long long kr = total_k > 0 ? total_k : 1;  // a map needs one row; no key row is read when total_k = 0
   if ((st = make_map(&tq, q, d, Hq, total_q, bm, "q")) != FA_OK) return st;
@@ -213,9 +212,8 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   p.causal = causal ? 1 : 0;
   p.window = window > 0 ? window : 0;
   p.err = di->status;
-  const int n_qtiles = (max_seqlen_q + bm - 1) / bm;
-  if (n_qtiles > 65535 || B > 65535) return fail(FA_ERR_INVALID, "grid too large");
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, n_qtiles, reinterpret_cast<cudaStream_t>(stream));
+  if (B > 65535) return fail(FA_ERR_INVALID, "grid too large");
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_seqlen_q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill (varlen) launch");
   return FA_OK;
 }

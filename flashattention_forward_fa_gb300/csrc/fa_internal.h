@@ -36,9 +36,10 @@ struct DecodeParams {
   uint32_t* err;
 };
 
+// max_rows: rows per sequence (padded layout) or the longest sequence (packed layout).
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int n_qtiles, cudaStream_t stream);
-int prefill_block_m();
+                           const PrefillParams& p, int max_rows, cudaStream_t stream);
+int prefill_box_rows();  // rows of one TMA box of Q / K / V
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           cudaStream_t stream);
