@@ -66,8 +66,8 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 0, 1);   // P K-major (TMEM), V MN-major
   // Registers per thread after the split (setmaxnreg): the softmax warpgroups grow, the
   // producer warpgroup shrinks.  Chosen so that neither side spills for either head dim.
-  static constexpr int REGS_SOFTMAX = (D == 128) ? 208 : 216;
-  static constexpr int REGS_PRODUCER = (D == 128) ? 72 : 56;
+  static constexpr int REGS_SOFTMAX = (D == 128) ? 200 : 208;
+  static constexpr int REGS_PRODUCER = (D == 128) ? 96 : 72;
   static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= THREADS * (65536 / THREADS / 8 * 8),
                 "register split exceeds the launch allocation");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -292,15 +292,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           if (!key_visible(k0 + j, pos, s.Lk, p.causal, p.window)) sc[j] = -INFINITY;
       }
       float mx;
-      {
-        float t8[8];
+      {  // row max: four independent chains of three-input max
+        float t4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) t8[u] = sc[u];
+        for (int u = 0; u < 4; ++u) t4[u] = sc[u];
 #pragma unroll
-        for (int j = 8; j < C::BN; j += 8)
+        for (int j = 4; j < C::BN - 4; j += 8)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[j + u]);
-        mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+          for (int u = 0; u < 4; ++u) t4[u] = fmax3(t4[u], sc[j + u], sc[j + 4 + u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) t4[u] = fmaxf(t4[u], sc[C::BN - 4 + u]);
+        mx = fmaxf(fmax3(t4[0], t4[1], t4[2]), t4[3]);
       }
       mx *= sl2;
       const float m_new = fmaxf(m, mx);
@@ -328,24 +330,32 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const float m_use = (m == -INFINITY) ? 0.f : m;
       // P V runs on bf16-rounded weights; normalising O by the sum of those same rounded
       // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
-      float rs0 = 0.f, rs1 = 0.f, rr0 = 0.f, rr1 = 0.f;
+      // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
+      // (two accumulators each to keep the dependency chains short).
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
+      uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      uint64_t lrs[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < C::BN / 32; ++c) {  // 32 scores -> 16 packed columns, stored at once
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float e0 = ex2_approx(fmaf(sc[32 * c + 2 * j], sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(sc[32 * c + 2 * j + 1], sl2, -m_use));
-          rs0 += e0;
-          rs1 += e1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sc[32 * c + 2 * j], sc[32 * c + 2 * j + 1]), sl2x2, negm2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
           pk[j] = pack_bf16x2(e0, e1);
-          rr0 += __uint_as_float(pk[j] << 16);
-          rr1 += __uint_as_float(pk[j] & 0xffff0000u);
+          lrs[j & 1] = f2_add(lrs[j & 1], f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u)));
         }
         tmem_st16(t_lane + colS + 16 * c, pk);
       }
-      l += rs0 + rs1;
-      lr += rr0 + rr1;
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
+        f2_unpack(f2_add(lrs[0], lrs[1]), b0, b1);
+        l += a0 + a1;
+        lr += b0 + b1;
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -435,29 +445,32 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     setmaxnreg_dec<C::REGS_PRODUCER>();
     if (lane == 0) {
-      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+      // Descriptors are built once; per MMA only the start-address field (bits 0..13, in 16-byte
+      // units) moves, by an offset that is a compile-time constant after unrolling.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::CHUNK, 1024);
       // S_X = Q_X K_i^T  (i = union index of the K tile)
       auto issue_s = [&](int X, int i) {
-        const uint32_t kb = k_base + (i % C::KST) * C::KV_BYTES;
-        const uint32_t qb = q_base + X * C::Q_BYTES;
+        const uint64_t kd = k_desc + (uint64_t)(((i % C::KST) * C::KV_BYTES) >> 4);
+        const uint64_t qd = q_desc + (uint64_t)((X * C::Q_BYTES) >> 4);
         const uint32_t d_cols = tmem + C::COL_S + 128u * X;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          umma_ss(d_cols, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), C::IDESC_S,
-                  kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((((kk >> 2) * C::CHUNK) + (kk & 3) * 32) >> 4);
+          umma_ss(d_cols, qd + off, kd + off, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[X]);
       };
       // O_X (+)= P_X V_i, P_X read from TMEM where the softmax left it
       auto issue_pv = [&](int X, int t, int i, const QTileRange& r) {
-        const uint32_t vb = v_base + (i % C::VST) * C::KV_BYTES;
+        const uint64_t vd = v_desc + (uint64_t)(((i % C::VST) * C::KV_BYTES) >> 4);
         const uint32_t p_cols = tmem + C::COL_S + 128u * X;
         const uint32_t d_cols = tmem + C::COL_O + (uint32_t)D * X;
+        const uint32_t acc0 = t > r.t0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(d_cols, p_cols + kk * 8, sdesc_sw128(vb + kk * 16 * 128, C::CHUNK, 1024), C::IDESC_O,
-                  (t > r.t0 || kk > 0) ? 1u : 0u);
+          umma_ts(d_cols, p_cols + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_O, kk > 0 ? 1u : acc0);
         if (t == r.t1 - 1) umma_commit(&o_final[X]);
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.err) && mbar_wait(&k_full[0], 0, abort_flag, p.err);
