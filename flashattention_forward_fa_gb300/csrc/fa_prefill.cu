@@ -443,84 +443,81 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop converged; one elected lane issues each instruction.
     setmaxnreg_dec<C::REGS_PRODUCER>();
-    if (lane == 0) {
-      // Descriptors are built once; per MMA only the start-address field (bits 0..13, in 16-byte
-      // units) moves, by an offset that is a compile-time constant after unrolling.
-      const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::CHUNK, 1024);
-      // S_X = Q_X K_i^T  (i = union index of the K tile)
-      auto issue_s = [&](int X, int i) {
-        const uint64_t kd = k_desc + (uint64_t)(((i % C::KST) * C::KV_BYTES) >> 4);
-        const uint64_t qd = q_desc + (uint64_t)((X * C::Q_BYTES) >> 4);
-        const uint32_t d_cols = tmem + C::COL_S + 128u * X;
+    const uint32_t leader = elect_one_sync() ? 1u : 0u;
+    // Descriptors are built once; per MMA only the start-address field (bits 0..13, in 16-byte
+    // units) moves, by an offset that is a compile-time constant after unrolling.
+    const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::CHUNK, 1024);
+    // S_X = Q_X K_i^T  (i = union index of the K tile)
+    auto issue_s = [&](int X, int i) {
+      const uint64_t kd = k_desc + (uint64_t)(((i % C::KST) * C::KV_BYTES) >> 4);
+      const uint64_t qd = q_desc + (uint64_t)((X * C::Q_BYTES) >> 4);
+      const uint32_t d_cols = tmem + C::COL_S + 128u * X;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)((((kk >> 2) * C::CHUNK) + (kk & 3) * 32) >> 4);
-          umma_ss(d_cols, qd + off, kd + off, C::IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[X]);
-      };
-      // O_X (+)= P_X V_i, P_X read from TMEM where the softmax left it
-      auto issue_pv = [&](int X, int t, int i, const QTileRange& r) {
-        const uint64_t vd = v_desc + (uint64_t)(((i % C::VST) * C::KV_BYTES) >> 4);
-        const uint32_t p_cols = tmem + C::COL_S + 128u * X;
-        const uint32_t d_cols = tmem + C::COL_O + (uint32_t)D * X;
-        const uint32_t acc0 = t > r.t0 ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(d_cols, p_cols + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_O, kk > 0 ? 1u : acc0);
-        if (t == r.t1 - 1) umma_commit(&o_final[X]);
-      };
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err) && mbar_wait(&k_full[0], 0, abort_flag, p.err);
-      if (ok) {
-        tc_fence_after();
-        if (act_a && ra.t0 == u0) issue_s(0, 0);
-        if (act_b && rb.t0 == u0) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)((((kk >> 2) * C::CHUNK) + (kk & 3) * 32) >> 4);
+        umma_ss_by(leader, d_cols, qd + off, kd + off, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
-      for (int t = u0; ok && t < u1; ++t) {
-        const int i = t - u0;
-        const bool nxt = t + 1 < u1;
-        bool v_ready = false, k_ready = false;
+      umma_commit_by(leader, &s_full[X]);
+    };
+    // O_X (+)= P_X V_i, P_X read from TMEM where the softmax left it
+    auto issue_pv = [&](int X, int t, int i, const QTileRange& r) {
+      const uint64_t vd = v_desc + (uint64_t)(((i % C::VST) * C::KV_BYTES) >> 4);
+      const uint32_t p_cols = tmem + C::COL_S + 128u * X;
+      const uint32_t d_cols = tmem + C::COL_O + (uint32_t)D * X;
+      const uint32_t acc0 = t > r.t0 ? 1u : 0u;
 #pragma unroll
-        for (int X = 0; X < C::NQT; ++X) {
-          const QTileRange& r = X ? rb : ra;
-          if (t >= r.t0 && t < r.t1) {
-            if (!mbar_wait(&p_full[X], (t - r.t0) & 1, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            if (!v_ready) {
-              if (!mbar_wait(&v_full[i % C::VST], (i / C::VST) & 1, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
-              v_ready = true;
-            }
-            tc_fence_after();
-            issue_pv(X, t, i, r);
-          }
-          if (nxt && t + 1 >= r.t0 && t + 1 < r.t1) {
-            if (!k_ready) {
-              if (!mbar_wait(&k_full[(i + 1) % C::KST], ((i + 1) / C::KST) & 1, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
-              k_ready = true;
-              tc_fence_after();
-            }
-            issue_s(X, i + 1);
-          }
-        }
-        if (!ok) break;
-        umma_commit(&v_empty[i % C::VST]);
-        if (nxt) umma_commit(&k_empty[(i + 1) % C::KST]);
-      }
-      umma_commit(mma_done);  // every MMA issued above has completed once this fires
-      mbar_wait(mma_done, 0, abort_flag, nullptr);
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        umma_ts_by(leader, d_cols, p_cols + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_O,
+                   kk > 0 ? 1u : acc0);
+      if (t == r.t1 - 1) umma_commit_by(leader, &o_final[X]);
+    };
+    bool ok = mbar_wait(bar_q, 0, abort_flag, p.err) && mbar_wait(&k_full[0], 0, abort_flag, p.err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      if (act_a && ra.t0 == u0) issue_s(0, 0);
+      if (act_b && rb.t0 == u0) issue_s(1, 0);
+      umma_commit_by(leader, &k_empty[0]);
     }
+    for (int t = u0; ok && t < u1; ++t) {
+      const int i = t - u0;
+      const bool nxt = t + 1 < u1;
+      bool v_ready = false, k_ready = false;
+#pragma unroll
+      for (int X = 0; X < C::NQT; ++X) {
+        const QTileRange& r = X ? rb : ra;
+        if (t >= r.t0 && t < r.t1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], (t - r.t0) & 1, abort_flag, p.err));
+          if (ok && !v_ready) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[i % C::VST], (i / C::VST) & 1, abort_flag, p.err));
+            v_ready = true;
+          }
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(X, t, i, r);
+        }
+        if (nxt && t + 1 >= r.t0 && t + 1 < r.t1) {
+          if (!k_ready) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&k_full[(i + 1) % C::KST], ((i + 1) / C::KST) & 1, abort_flag, p.err));
+            if (!ok) break;
+            k_ready = true;
+            tc_fence_after();
+          }
+          issue_s(X, i + 1);
+        }
+      }
+      if (!ok) break;
+      umma_commit_by(leader, &v_empty[i % C::VST]);
+      if (nxt) umma_commit_by(leader, &k_empty[(i + 1) % C::KST]);
+    }
+    umma_commit_by(leader, mma_done);  // every MMA issued above has completed once this fires
+    mbar_wait(mma_done, 0, abort_flag, nullptr);
+    __syncwarp();
   } else {
     setmaxnreg_dec<C::REGS_PRODUCER>();  // warp 11: idle, its registers go to the softmax warps
   }
