@@ -292,17 +292,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           if (!key_visible(k0 + j, pos, s.Lk, p.causal, p.window)) sc[j] = -INFINITY;
       }
       float mx;
-      {  // row max: four independent chains of three-input max
-        float t4[4];
+      {  // row max: eight independent chains of three-input max
+        float t8[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) t4[u] = sc[u];
+        for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
 #pragma unroll
-        for (int j = 4; j < C::BN - 4; j += 8)
+        for (int j = 24; j < C::BN - 8; j += 16)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) t4[u] = fmax3(t4[u], sc[j + u], sc[j + 4 + u]);
+          for (int u = 0; u < 8; ++u) t8[u] = fmax3(t8[u], sc[j + u], sc[j + 8 + u]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) t4[u] = fmaxf(t4[u], sc[C::BN - 4 + u]);
-        mx = fmaxf(fmax3(t4[0], t4[1], t4[2]), t4[3]);
+        for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
+        mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
       }
       mx *= sl2;
       const float m_new = fmaxf(m, mx);
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       // (two accumulators each to keep the dependency chains short).
       const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
       uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-      uint64_t lrs[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+      float lr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < C::BN / 32; ++c) {  // 32 scores -> 16 packed columns, stored at once
         uint32_t pk[16];
@@ -345,16 +345,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
           ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
           pk[j] = pack_bf16x2(e0, e1);
-          lrs[j & 1] = f2_add(lrs[j & 1], f2_pack(__uint_as_float(pk[j] << 16), __uint_as_float(pk[j] & 0xffff0000u)));
+          bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
         }
         tmem_st16(t_lane + colS + 16 * c, pk);
       }
       {
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
-        f2_unpack(f2_add(lrs[0], lrs[1]), b0, b1);
         l += a0 + a1;
-        lr += b0 + b1;
+        lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
       }
       tmem_st_wait();
       tc_fence_before();

@@ -286,6 +286,13 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// a += (float)lo16(w), b += (float)hi16(w): accumulate the two bf16 halves of a packed word in fp32.
+__device__ __forceinline__ void bf16x2_accumulate(float& a, float& b, uint32_t w) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "r"(w));
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
