@@ -68,11 +68,17 @@ def _check(status: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(t: torch.Tensor):
-    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    # The raw handle of torch's current stream on t's device (the fast accessor when present).
+    if _raw_stream is not None:
+        return _raw_stream(t.device.index)
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _host_ints(x) -> Optional[ctypes.Array]:
@@ -83,12 +89,13 @@ def _host_ints(x) -> Optional[ctypes.Array]:
 
 
 def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous():
+        return
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise FAError(FA_ERR_INVALID, f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise FAError(FA_ERR_INVALID, f"{name} must be {dtype}")
-    if not t.is_contiguous():
-        raise FAError(FA_ERR_INVALID, f"{name} must be contiguous")
+    raise FAError(FA_ERR_INVALID, f"{name} must be contiguous")
 
 
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, window: int = 0,

@@ -90,8 +90,8 @@ fa_status get_encoder() {
 
 // 3-D view [rows, heads, d] of a row-major bf16 tensor; box = 64 columns x 1 head x box_rows rows,
 // 128-byte swizzle (the layout the kernels' shared-memory descriptors assume).
-fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows, int box_rows,
-                   const char* name) {
+fa_status encode_map(CUtensorMap* map, const void* base, int d, int heads, long long rows, int box_rows,
+                     const char* name) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
@@ -100,6 +100,41 @@ fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long lo
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return FA_OK;
+}
+
+// Encoding a descriptor is a host call of a few microseconds; repeated calls on the same tensors
+// (the usual case: one layer called step after step) reuse a small per-thread cache.  A descriptor
+// depends only on the address, sizes and box, so a hit is always valid.
+struct MapCacheEntry {
+  const void* base = nullptr;
+  int d = 0, heads = 0, box_rows = 0;
+  long long rows = 0;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+thread_local MapCacheEntry t_map_cache[kMapCache];
+thread_local int t_map_next = 0;
+
+fa_status make_map(CUtensorMap* map, const void* base, int d, int heads, long long rows, int box_rows,
+                   const char* name) {
+  for (int i = 0; i < kMapCache; ++i) {
+    const MapCacheEntry& e = t_map_cache[i];
+    if (e.base == base && e.d == d && e.heads == heads && e.rows == rows && e.box_rows == box_rows) {
+      *map = e.map;
+      return FA_OK;
+    }
+  }
+  fa_status st = encode_map(map, base, d, heads, rows, box_rows, name);
+  if (st != FA_OK) return st;
+  MapCacheEntry& e = t_map_cache[t_map_next];
+  t_map_next = (t_map_next + 1) % kMapCache;
+  e.base = base;
+  e.d = d;
+  e.heads = heads;
+  e.rows = rows;
+  e.box_rows = box_rows;
+  e.map = *map;
   return FA_OK;
 }
 

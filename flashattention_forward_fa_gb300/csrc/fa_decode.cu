@@ -372,9 +372,16 @@ template <int D>
 static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                    cudaStream_t stream) {
   using C = DecodeCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  static int attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fa_decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
   const int n_rb = (p.group + 15) / 16;
   dim3 grid(p.max_splits, p.Hkv * n_rb, p.B);
   fa_decode_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);

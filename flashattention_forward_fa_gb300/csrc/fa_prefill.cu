@@ -532,9 +532,16 @@ template <int D>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, int max_rows, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  static int attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
   const int rows_per_cta = C::NQT * C::BM;
   dim3 grid(p.Hq, (max_rows + rows_per_cta - 1) / rows_per_cta, p.B);
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
