@@ -141,15 +141,16 @@ __device__ __forceinline__ bool tile_needs_mask(const QTileRange& r, int k0, int
   return m;
 }
 
-__device__ __forceinline__ bool key_visible(int key, int pos, int Lk, int causal, int window) {
-  bool ok = key < Lk;
-  if (causal) {
-    ok = ok && key <= pos;
-    if (window > 0) ok = ok && key > pos - window;
-  } else if (window > 0) {
-    ok = ok && key > pos - window && key < pos + window;
+// The keys row position `pos` may see form one interval [lo, hi): causal keeps j <= pos, a
+// window keeps j > pos - window (and, without causal, j < pos + window), every row keeps j < Lk.
+__device__ __forceinline__ void visible_keys(int pos, int Lk, int causal, int window, int& lo, int& hi) {
+  lo = 0;
+  hi = Lk;
+  if (causal) hi = min(hi, pos + 1);
+  if (window > 0) {
+    lo = max(lo, pos - window + 1);
+    if (!causal) hi = min(hi, pos + window);
   }
-  return ok;
 }
 
 template <int D>
@@ -251,6 +252,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     const int rg = tid & 127;              // row within the tile = TMEM lane
     const int i = r.q0 + rg;
     const int pos = i + s.Lk - s.Lq;
+    int row_lo, row_hi;  // this row's visible keys [row_lo, row_hi)
+    visible_keys(pos, s.Lk, p.causal, p.window, row_lo, row_hi);
     const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t colS = C::COL_S + 128u * X, colO = C::COL_O + (uint32_t)D * X;
     const float sl2 = p.scale_log2;
@@ -287,9 +290,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
       const int k0 = t * C::BN;
       if (tile_needs_mask<C::BN>(r, k0, s.Lk, p.causal, p.window)) {
+        // keep column j iff k0 + j lies in the row's visible interval: one unsigned compare per key
+        const uint32_t lo = (uint32_t)(row_lo - k0);
+        const uint32_t span = (uint32_t)max(row_hi - row_lo, 0);
 #pragma unroll
         for (int j = 0; j < C::BN; ++j)
-          if (!key_visible(k0 + j, pos, s.Lk, p.causal, p.window)) sc[j] = -INFINITY;
+          if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
       }
       float mx;
       {  // row max: eight independent chains of three-input max
