@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
 * ``fa_fwd(q, k, v, ...)``         padded-batch prefill   q [B, Nq, Hq, d]
 * ``fa_fwd_varlen(q, k, v, ...)``  packed varlen prefill  q [total_q, Hq, d]
 * ``fa_decode(q, k_cache, v_cache, seqlens_k, ...)``  one new token per sequence
+* ``fa_decode_paged(...)``         decode over a paged (block-table) KV cache
 * ``fa_decode_noalloc(...)``       the same decode with no device allocation at all
 * ``fa_device_status()``           read/clear the kernels' error word
 """
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     fa_decode,
     fa_decode_max_splits,
     fa_decode_noalloc,
+    fa_decode_paged,
     fa_device_status,
     fa_fwd,
     fa_fwd_varlen,
@@ -36,6 +38,7 @@ __all__ = [
     "fa_decode",
     "fa_decode_max_splits",
     "fa_decode_noalloc",
+    "fa_decode_paged",
     "decode_workspace_size",
     "fa_device_status",
     "load_library",

@@ -28,6 +28,8 @@ _SIGS = {
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp, _sz, _vp]),
     "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _ip, _i]),
+    "fa_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _ip, _i, _vp,
+                             _sz, _vp]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
@@ -195,6 +197,42 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
                          int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(q)))
+    return o, lse
+
+
+def fa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                    seqlens_k: torch.Tensor, window: int = 0, scale: Optional[float] = None, num_splits: int = 0,
+                    seqlens_k_host=None, workspace: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode over a paged cache: q [B, Hq, d], pages [num_pages, page_size, Hkv, d],
+    block_table int32 [B, max_blocks], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
+    lib = load_library()
+    _need(q, "q")
+    _need(k_pages, "k_pages")
+    _need(v_pages, "v_pages")
+    _need(block_table, "block_table", torch.int32)
+    _need(seqlens_k, "seqlens_k", torch.int32)
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.shape != k_pages.shape or block_table.dim() != 2:
+        raise FAError(FA_ERR_INVALID, "expected q [B,Hq,d], pages [P,page,Hkv,d], block_table [B,max_blocks]")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_blocks = block_table.shape[1]
+    host = _host_ints(seqlens_k_host)
+    hostp = ctypes.cast(host, _ip) if host is not None else None
+    if workspace is None:
+        S = lib.fa_decode_max_splits(B, Hq, Hkv, max_blocks * page_size, int(window) + 63 if window > 0 else 0,
+                                     hostp, int(num_splits))
+        nbytes = lib.fa_decode_workspace_size(B, Hq, d, max(S, 1))
+        workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=q.device)
+    o = out if out is not None else torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(o), _ptr(lse), B, Hq, Hkv, num_pages,
+                               page_size, d, sc, int(window), _ptr(block_table), max_blocks, _ptr(seqlens_k), hostp,
+                               int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(q)))
     return o, lse
 
 

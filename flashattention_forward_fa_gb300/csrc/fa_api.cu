@@ -361,6 +361,63 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, voi
   return FA_OK;
 }
 
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, float* lse, int B,
+                          int Hq, int Hkv, int num_pages, int page_size, int d, float scale, int window,
+                          const int* block_table, int max_blocks, const int* seqlens_k, const int* seqlens_k_host,
+                          int num_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  fa_status st = check_common(q, k_pages, v_pages, o, lse, B, Hq, Hkv, d, scale);
+  if (st != FA_OK) return st;
+  if (!seqlens_k || !block_table) return fail(FA_ERR_INVALID, "seqlens_k and block_table must be non-null");
+  if (page_size <= 0 || page_size % 64 != 0)
+    return fail(FA_ERR_INVALID, "page_size (%d) must be a positive multiple of 64", page_size);
+  if (num_pages <= 0 || max_blocks <= 0) return fail(FA_ERR_INVALID, "num_pages and max_blocks must be positive");
+  if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_blocks * page_size >= (1LL << 30))
+    return fail(FA_ERR_INVALID, "paged cache too large");
+  if (num_splits < 0) return fail(FA_ERR_INVALID, "num_splits must be >= 0");
+  if (B > 65535) return fail(FA_ERR_INVALID, "B too large");
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const int cap = max_blocks * page_size;
+  // chunks start on a 64-key boundary at or below the window start: plan with window + 63
+  const int plan_window = window > 0 ? window + 63 : 0;
+  const DecodePlan pl = plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, seqlens_k_host, num_splits, di->sm_count);
+  const size_t need = fa_decode_workspace_size(B, Hq, d, pl.max_splits);
+  if (!workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
+  if (!aligned16(workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (pl.max_splits > 65535) return fail(FA_ERR_INVALID, "too many splits");
+  if ((st = get_encoder()) != FA_OK) return st;
+  CUtensorMap tk, tv;
+  const int bn = fa::decode_block_n();
+  if ((st = make_map(&tk, k_pages, d, Hkv, (long long)num_pages * page_size, bn, "k_pages")) != FA_OK) return st;
+  if ((st = make_map(&tv, v_pages, d, Hkv, (long long)num_pages * page_size, bn, "v_pages")) != FA_OK) return st;
+  fa::DecodeParams p{};
+  p.q = q;
+  p.o = o;
+  p.lse = lse;
+  p.seqlens_k = seqlens_k;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = p.o_part + (size_t)B * Hq * pl.max_splits * d;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Ncap = cap;
+  p.group = Hq / Hkv;
+  p.chunk = pl.chunk;
+  p.max_splits = pl.max_splits;
+  p.window = window > 0 ? window : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.err = di->status;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  cudaError_t e = fa::launch_decode(d, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  return FA_OK;
+}
+
 fa_status fa_device_status(uint32_t* bits, int clear) {
   DeviceInfo* di = nullptr;
   fa_status st = device_info(&di);

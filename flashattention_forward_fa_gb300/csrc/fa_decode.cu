@@ -70,11 +70,38 @@ __device__ __forceinline__ uint32_t sw_off(int key, int d8) {
   return (uint32_t)((d8 >> 3) * DecodeCfg<D>::SLAB + key * 128 + (((d8 & 7) ^ (key & 7)) << 4));
 }
 
+// Key range of sequence b: [lo, len) are the keys its query may see; the chunks cover
+// [base, len) with base = lo for a contiguous cache and lo rounded down to a multiple of 64 for
+// a paged one (so that no 64-key tile straddles two pages; keys below lo are then masked).
+struct DecodeRange {
+  int len, lo, base;
+};
+__device__ __forceinline__ DecodeRange decode_range(const DecodeParams& p, int b, bool paged) {
+  DecodeRange r;
+  const int cap = paged ? p.max_blocks * p.page_size : p.Ncap;
+  r.len = min(max(p.seqlens_k[b], 0), cap);
+  r.lo = p.window > 0 ? max(0, r.len - p.window) : 0;
+  r.base = paged ? (r.lo & ~63) : r.lo;
+  return r;
+}
+
+// Physical row of the first key of a 64-key tile.  A block-table entry outside [0, num_pages)
+// is recorded in the device status word and replaced by page 0, so a bad table cannot fault.
+__device__ __forceinline__ int paged_row(const DecodeParams& p, int b, int key) {
+  const int blk = key / p.page_size;
+  int page = (blk < p.max_blocks) ? p.block_table[(size_t)b * p.max_blocks + blk] : -1;
+  if (page < 0 || page >= p.num_pages) {
+    atomicOr(p.err, kDevErrBounds);
+    page = 0;
+  }
+  return page * p.page_size + (key - blk * p.page_size);
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
@@ -85,9 +112,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
   const int hkv = blockIdx.y / n_rb;
   const int rb = blockIdx.y % n_rb;
   const int b = blockIdx.z;
-  const int len = min(max(p.seqlens_k[b], 0), p.Ncap);
-  const int lo = p.window > 0 ? max(0, len - p.window) : 0;
-  const int start = lo + split * p.chunk;
+  const DecodeRange kr = decode_range(p, b, PAGED);
+  const int len = kr.len, lo = kr.lo;
+  const int start = kr.base + split * p.chunk;
   const int end = min(start + p.chunk, len);
   if (start >= end) return;  // chunk past the end of this sequence's keys
   const int n_tiles = (end - start + C::BN - 1) / C::BN;
@@ -117,12 +144,15 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int t = 0;
+      // paged: the next tile's page is looked up one tile ahead, hiding the table load
+      int row_next = PAGED ? paged_row(p, b, start) : 0;
       for (; t < n_tiles; ++t) {
         const int st = t % C::ST;
+        const int row = PAGED ? row_next : b * p.Ncap + start + t * C::BN;
+        if (PAGED && t + 1 < n_tiles) row_next = paged_row(p, b, start + (t + 1) * C::BN);
         if (t >= C::ST && !mbar_wait(&empty[st], ((t / C::ST) + 1) & 1, abort_flag, p.err)) break;
         mbar_arrive_expect_tx(&full[st], C::STAGE);
         uint8_t* dst = sm + st * C::STAGE;
-        const int row = b * p.Ncap + start + t * C::BN;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d(dst + c * C::SLAB, &tm_k, &full[st], c * 64, hkv, row);
@@ -173,6 +203,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
     }
     const int kb = warp * 16;                              // this warp's keys within the tile
     const int nvalid = min(16, end - (start + t * C::BN + kb));
+    const int nlow = PAGED ? lo - (start + t * C::BN + kb) : 0;  // keys below the window start
     const uint32_t kaddr = sbase + st * C::STAGE;
     const uint32_t vaddr = kaddr + C::TILE;
     if (nvalid > 0) {
@@ -201,7 +232,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (n * 8 + 2 * tq + (e & 1) >= nvalid) sc[n][e] = -INFINITY;
+          if (n * 8 + 2 * tq + (e & 1) >= nvalid || (PAGED && n * 8 + 2 * tq + (e & 1) < nlow))
+            sc[n][e] = -INFINITY;
       float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -320,9 +352,9 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.B * p.Hq) return;
   const int b = warp_global / p.Hq, hq = warp_global % p.Hq;
-  const int len = min(max(p.seqlens_k[b], 0), p.Ncap);
-  const int lo = p.window > 0 ? max(0, len - p.window) : 0;
-  const int nkeys = len - lo;
+  const DecodeRange kr = decode_range(p, b, p.page_size > 0);
+  const int nkeys = kr.len - kr.lo;
+  const int nspan = kr.len - kr.base;  // keys the chunks cover
   constexpr int PER = D / 32;  // output columns per lane
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)b * p.Hq + hq) * D + lane * PER;
   if (nkeys <= 0) {
@@ -331,7 +363,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = -INFINITY;
     return;
   }
-  const int ns = min((nkeys + p.chunk - 1) / p.chunk, p.max_splits);  // never read past the workspace
+  const int ns = min((nspan + p.chunk - 1) / p.chunk, p.max_splits);  // never read past the workspace
   const size_t prow0 = ((size_t)b * p.Hq + hq) * p.max_splits;
   constexpr float LOG2E = 1.4426950408889634f;
   float mx = -INFINITY;
@@ -368,7 +400,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = mx + __logf(tot);
 }
 
-template <int D>
+template <int D, bool PAGED>
 static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                    cudaStream_t stream) {
   using C = DecodeCfg<D>;
@@ -378,13 +410,14 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fa_decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   const int n_rb = (p.group + 15) / 16;
   dim3 grid(p.max_splits, p.Hkv * n_rb, p.B);
-  fa_decode_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
+  fa_decode_split_kernel<D, PAGED><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = p.B * p.Hq;
@@ -394,8 +427,9 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           cudaStream_t stream) {
-  if (d == 64) return launch_decode_d<64>(tk, tv, p, stream);
-  return launch_decode_d<128>(tk, tv, p, stream);
+  const bool paged = p.page_size > 0;
+  if (d == 64) return paged ? launch_decode_d<64, true>(tk, tv, p, stream) : launch_decode_d<64, false>(tk, tv, p, stream);
+  return paged ? launch_decode_d<128, true>(tk, tv, p, stream) : launch_decode_d<128, false>(tk, tv, p, stream);
 }
 
 int decode_block_n() { return DecodeCfg<128>::BN; }

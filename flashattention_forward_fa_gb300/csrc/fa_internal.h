@@ -34,6 +34,10 @@ struct DecodeParams {
   int window;
   float scale_log2;
   uint32_t* err;
+  // paged cache (page_size > 0): k/v are [num_pages, page_size, Hkv, d] and key j of sequence b
+  // lives in page block_table[b * max_blocks + j / page_size]; page_size is a multiple of 64.
+  const int* block_table;
+  int max_blocks, page_size, num_pages;
 };
 
 // max_rows: rows per sequence (padded layout) or the longest sequence (packed layout).
@@ -42,7 +46,7 @@ cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, 
 int prefill_box_rows();  // rows of one TMA box of Q / K / V
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                          cudaStream_t stream);
+                          cudaStream_t stream);  // paged when p.page_size > 0
 int decode_block_n();
 
 }  // namespace fa

@@ -131,6 +131,28 @@ FA_API fa_status fa_decode(const void* q, const void* k_cache, const void* v_cac
                     fa_stream_t stream);
 
 /*
+ * Single-query decode over a paged KV cache (the plain gather of a block-table
+ * KV cache: hwcomputing.csdn.net page, §4.1 "KV Cache内存优化", without its
+ * importance-based selection).  As fa_decode, except for the cache layout:
+ *   k_pages, v_pages : [num_pages, page_size, Hkv, d] bf16
+ *   block_table : device int32 [B, max_blocks]; key j of sequence b lives in
+ *       page block_table[b * max_blocks + j / page_size], row j % page_size
+ *   page_size : a positive multiple of 64 (one 64-key tile never straddles pages)
+ *   seqlens_k : device int32 [B], values clamped to [0, max_blocks * page_size]
+ * A table entry outside [0, num_pages) sets bit 1 of the device status word
+ * (fa_device_status) and reads page 0 instead; it cannot fault.
+ * Workspace: fa_decode_workspace_size(B, Hq, d, S) with
+ *   S = fa_decode_max_splits(B, Hq, Hkv, max_blocks * page_size,
+ *                            window > 0 ? window + 63 : 0, seqlens_k_host, num_splits).
+ */
+FA_API fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, float* lse,
+                                 int B, int Hq, int Hkv, int num_pages, int page_size, int d, float scale,
+                                 int window, const int* block_table, int max_blocks,
+                                 const int* seqlens_k, const int* seqlens_k_host,
+                                 int num_splits, void* workspace, size_t workspace_bytes,
+                                 fa_stream_t stream);
+
+/*
  * The split bound S that fa_decode uses for the same arguments on the current
  * device (size the workspace with fa_decode_workspace_size(B, Hq, d, S)).
  * Returns 0 for invalid sizes.

@@ -140,3 +140,19 @@ def test_binding_fails_loudly_without_cuda_tensors():
     q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(b.FAError):
         fa.fa_fwd(q, q, q)
+
+
+def test_paged_decode_arguments_checked(lib):
+    _, b = _binding()
+    L = b.load_library()
+    d = ctypes.c_void_p(0x1000)
+    args = lambda **kw: [kw.get("q", d), d, d, d, None, 2, 8, 2, kw.get("num_pages", 10), kw.get("page", 64), 128,
+                         ctypes.c_float(0.1), 0, kw.get("table", d), kw.get("max_blocks", 4), kw.get("lens", d), None,
+                         0, d, 1 << 24, None]
+    assert L.fa_decode_paged(*args(page=96)) == 1            # not a multiple of 64
+    assert b"multiple of 64" in L.fa_last_error()
+    assert L.fa_decode_paged(*args(page=0)) == 1
+    assert L.fa_decode_paged(*args(table=None)) == 1
+    assert L.fa_decode_paged(*args(lens=None)) == 1
+    assert L.fa_decode_paged(*args(num_pages=0)) == 1
+    assert L.fa_decode_paged(*args(max_blocks=0)) == 1
