@@ -69,12 +69,13 @@ def _ptr(a: np.ndarray):
 
 def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
                    q_off, len_q, k_off, len_k, scale: float, causal: bool, window: int,
-                   rows: np.ndarray, threads: int = 0):
+                   rows: np.ndarray, threads: int = 0, alibi_slopes=None):
     """Selected rows of attention, in fp64, from bf16 bit patterns.
 
     q_bits [Tq, Hq, d] uint16, k_bits/v_bits [Tk, Hkv, d] uint16 (row-major).
     Sequence b occupies q rows q_off[b] .. q_off[b]+len_q[b]-1 (same for k).
     rows: int array [n, 3] of (b, h, i).  Returns (O [n, d], LSE [n]) float64.
+    alibi_slopes: optional per-query-head slopes m_h; the score gets -m_h |p - j|.
     """
     lib = _load()
     # leading dims are flattened into rows: [..., H, d] -> [rows, H, d]
@@ -93,6 +94,9 @@ def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     len_k = np.ascontiguousarray(len_k, dtype=np.int32)
     rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
     n = rows.shape[0]
+    slopes = None if alibi_slopes is None else np.ascontiguousarray(alibi_slopes, dtype=np.float64)
+    if slopes is not None and slopes.shape != (hq,):
+        raise ValueError("alibi_slopes must have one slope per query head")
     o = np.zeros((n, d), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     rc = lib.oracle_attention_rows(
@@ -100,6 +104,7 @@ def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
         ctypes.c_int(B), ctypes.c_int(hq), ctypes.c_int(hkv), ctypes.c_int(d),
         _ptr(q_off), _ptr(len_q), _ptr(k_off), _ptr(len_k),
         ctypes.c_double(scale), ctypes.c_int(int(bool(causal))), ctypes.c_int(int(window)),
+        _ptr(slopes) if slopes is not None else None,
         ctypes.c_int(n), _ptr(rows), _ptr(o), _ptr(lse), ctypes.c_int(int(threads)))
     if rc != 0:
         raise ValueError("oracle_attention_rows: bad arguments or out of memory")

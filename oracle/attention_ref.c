@@ -27,6 +27,10 @@
  *  - a row with no allowed key has O = 0 and LSE = -inf (log of an empty sum);
  *  - LSE is the natural log of the row's normaliser in scaled-score units,
  *    LSE_i = M_i + ln(sum_j exp(s_ij - M_i)).
+ *  - ALiBi (optional): the jsqmd page, §三 "ALiBi位置编码的线性偏置", adds -m * |i - j|
+ *    to each scaled score, m a per-head slope; the pages give no slope values, so
+ *    the caller passes them, and i is the query's absolute position p (the same
+ *    bottom-right alignment as the causal mask): s_ij = scale q.k - m_h |p - j|.
  *
  * Inputs are raw bf16 bit patterns (uint16); bf16 -> fp64 is exact.
  */
@@ -66,6 +70,7 @@ static int key_allowed(long p, long j, int causal, int window) {
  *  q      bf16 bits, row r of sequence b at element ((q_off[b] + r) * Hq + h) * d
  *  k, v   bf16 bits, row j of sequence b at element ((k_off[b] + j) * Hkv + g) * d
  *  len_q, len_k   per-sequence valid lengths
+ *  alibi_slopes  NULL, or Hq per-head slopes m_h (bias -m_h |p - j| on the scaled score)
  *  rows   n_rows triples (b, h, i)
  *  o_out  [n_rows, d] fp64;  lse_out [n_rows] fp64
  *  work   scratch of n_threads * max_len_k doubles is allocated internally
@@ -76,7 +81,7 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           int B, int Hq, int Hkv, int d,
                           const long* q_off, const int* len_q,
                           const long* k_off, const int* len_k,
-                          double scale, int causal, int window,
+                          double scale, int causal, int window, const double* alibi_slopes,
                           int n_rows, const int* rows_bhi,
                           double* o_out, double* lse_out, int n_threads) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
@@ -117,6 +122,7 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
         double dot = 0.0;
         for (int t = 0; t < d; ++t) dot += bf16_to_f64(qi[t]) * bf16_to_f64(kj[t]);
         s[j] = scale * dot;
+        if (alibi_slopes) s[j] -= alibi_slopes[h] * fabs((double)(p - j));
         if (!any || s[j] > M) M = s[j];
         any = 1;
       }

@@ -47,9 +47,11 @@ def visible_mask(lq: int, lk: int, causal: bool, window: int) -> np.ndarray:
 
 
 def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-              causal: bool = False, window: int = 0):
+              causal: bool = False, window: int = 0, alibi_slopes=None):
     """One sequence.  q [lq, Hq, d], k/v [lk, Hkv, d] (float64).
 
+    alibi_slopes: optional [Hq] slopes; the jsqmd page's ALiBi (§三) adds -m_h |p - j|
+    to each scaled score, p the query's absolute position (bottom-right aligned).
     Returns O [lq, Hq, d] and LSE [Hq, lq] (float64).
     """
     lq, hq, d = q.shape
@@ -57,11 +59,14 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     assert hq % hkv == 0
     group = hq // hkv
     vis = visible_mask(lq, lk, causal, window)
+    dist = np.abs((np.arange(lq)[:, None] + (lk - lq)) - np.arange(lk)[None, :]).astype(np.float64)
     o = np.zeros((lq, hq, d))
     lse = np.full((hq, lq), -np.inf)
     for h in range(hq):
         g = h // group
         s = (q[:, h, :] @ k[:, g, :].T) * scale          # [lq, lk]
+        if alibi_slopes is not None:
+            s = s - alibi_slopes[h] * dist
         s = np.where(vis, s, -np.inf)
         has_key = vis.any(axis=1)
         m = np.where(has_key, s.max(axis=1, initial=-np.inf), 0.0)

@@ -367,3 +367,90 @@ MUTANTS = {
 @pytest.mark.parametrize("name", list(MUTANTS))
 def test_planted_mistakes_are_caught(name):
     assert _pins(MUTANTS[name]) != [], f"pins did not catch: {name}"
+
+
+# ----------------------------------------------------------------------------- ALiBi
+
+def brute_force_alibi(q, k, v, scale, causal, window, slopes):
+    """Scalar loops: score = scale q.k - m_h |p - j|, p = i + lk - lq (written independently)."""
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    lq, hq, d = qd.shape
+    lk, hkv, _ = kd.shape
+    O = np.zeros((lq, hq, d))
+    L = np.full((hq, lq), -np.inf)
+    for h in range(hq):
+        g = h * hkv // hq
+        for i in range(lq):
+            pos = i + lk - lq
+            keys = [j for j in range(lk)
+                    if not (causal and (j > pos or (window > 0 and pos - j >= window)))
+                    and not (not causal and window > 0 and abs(pos - j) >= window)]
+            if not keys:
+                continue
+            sc = [scale * sum(qd[i, h, t] * kd[j, g, t] for t in range(d)) - slopes[h] * abs(pos - j) for j in keys]
+            m = max(sc)
+            w = [math.exp(s - m) for s in sc]
+            z = sum(w)
+            for t in range(d):
+                O[i, h, t] = sum(w[n] * vd[keys[n], g, t] for n in range(len(keys))) / z
+            L[h, i] = m + math.log(z)
+    return O, L
+
+
+def c_oracle_alibi(q, k, v, scale, causal, window, slopes):
+    lq, hq, d = q.shape
+    rows = oracle.all_rows([lq], hq)
+    o, lse = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), [0], [lq], [0], [k.shape[0]],
+                                   scale, causal, window, rows, alibi_slopes=slopes)
+    O = np.zeros((lq, hq, d))
+    L = np.full((hq, lq), -np.inf)
+    for n, (_, h, i) in enumerate(rows):
+        O[i, h] = o[n]
+        L[h, i] = lse[n]
+    return O, L
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_alibi_c_numpy_bruteforce_agree(mode):
+    lq, lk, hq, hkv, d, causal, window = mode
+    q, k, v = rand_seq(lq, lk, hq, hkv, d)
+    slopes = np.array([0.5 ** (h + 1) for h in range(hq)])
+    Oc, Lc = c_oracle_alibi(q, k, v, 0.4, causal, window, slopes)
+    On, Ln = ref_numpy.attention(f64(q), f64(k), f64(v), 0.4, causal, window, alibi_slopes=slopes)
+    Ob, Lb = brute_force_alibi(q, k, v, 0.4, causal, window, slopes)
+    fin = np.isfinite(Lb)
+    for O, L in ((Oc, Lc), (On, Ln)):
+        np.testing.assert_allclose(O, Ob, rtol=0, atol=1e-12)
+        assert np.array_equal(np.isfinite(L), fin)
+        np.testing.assert_allclose(L[fin], Lb[fin], rtol=0, atol=1e-12)
+
+
+def test_alibi_zero_query_gives_geometric_weights():
+    # q = 0, causal, Nq = Nk: row i weights key j by r^(i - j), r = exp(-m)
+    n, d, m = 9, 4, 0.7
+    q = to_bf16(np.zeros((n, 1, d)))
+    k = to_bf16(RNG.standard_normal((n, 1, d)))
+    v = to_bf16(RNG.standard_normal((n, 1, d)))
+    O, L = c_oracle_alibi(q, k, v, 1.0, True, 0, np.array([m]))
+    r = math.exp(-m)
+    for i in range(n):
+        w = np.array([r ** (i - j) for j in range(i + 1)])
+        np.testing.assert_allclose(O[i, 0], (w[:, None] * f64(v)[: i + 1, 0]).sum(0) / w.sum(), atol=1e-12)
+        assert abs(L[0, i] - math.log((1 - r ** (i + 1)) / (1 - r))) < 1e-12
+
+
+def test_alibi_zero_slope_is_plain_attention():
+    q, k, v = rand_seq(6, 11, 4, 2, 8)
+    for causal in (False, True):
+        O1, L1 = c_oracle_alibi(q, k, v, 0.3, causal, 0, np.zeros(4))
+        O2, L2 = c_oracle_seq(q, k, v, 0.3, causal, 0)
+        np.testing.assert_array_equal(O1, O2)
+        np.testing.assert_array_equal(L1, L2)
+
+
+def test_alibi_sign_mistake_is_caught():
+    q, k, v = rand_seq(5, 8, 2, 2, 4)
+    slopes = np.array([0.25, 0.5])
+    Ob, Lb = brute_force_alibi(q, k, v, 0.5, True, 0, slopes)
+    Om, Lm = c_oracle_alibi(q, k, v, 0.5, True, 0, -slopes)    # planted: bias added with the wrong sign
+    assert not np.allclose(Om, Ob, atol=1e-6)
