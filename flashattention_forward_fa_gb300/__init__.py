@@ -12,13 +12,18 @@ Entry points (same names as the C ABI):
 * ``fa_decode(q, k_cache, v_cache, seqlens_k, ...)``  one new token per sequence
 * ``fa_decode_paged(...)``         decode over a paged (block-table) KV cache
 * ``fa_decode_noalloc(...)``       the same decode with no device allocation at all
+* ``fa_fwd_ex`` / ``fa_decode_ex`` (C ABI): every option in one struct; reached from
+  the wrappers above when ``alibi_slopes`` is given
 * ``fa_device_status()``           read/clear the kernels' error word
 """
 
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    DecodeArgs,
     FAError,
+    FwdArgs,
+    alibi_slopes,
     decode_workspace_size,
     fa_decode,
     fa_decode_max_splits,
@@ -33,6 +38,9 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "FAError",
+    "FwdArgs",
+    "DecodeArgs",
+    "alibi_slopes",
     "fa_fwd",
     "fa_fwd_varlen",
     "fa_decode",

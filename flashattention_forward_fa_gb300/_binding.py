@@ -21,6 +21,24 @@ _NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_C
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _ip = ctypes.POINTER(ctypes.c_int)
 
+class FwdArgs(ctypes.Structure):
+    """Mirror of fa_fwd_args (include/fa.h)."""
+    _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
+                ("B", _i), ("Hq", _i), ("Hkv", _i), ("Nq", _i), ("Nk", _i), ("d", _i),
+                ("scale", _f), ("causal", _i), ("window", _i),
+                ("seqlens_q", _vp), ("seqlens_k", _vp), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
+                ("total_q", _i), ("total_k", _i), ("cu_seqlens_q_host", _ip), ("alibi_slopes", _vp)]
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of fa_decode_args (include/fa.h)."""
+    _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
+                ("B", _i), ("Hq", _i), ("Hkv", _i), ("d", _i), ("scale", _f), ("window", _i), ("Ncap", _i),
+                ("block_table", _vp), ("max_blocks", _i), ("page_size", _i), ("num_pages", _i),
+                ("seqlens_k", _vp), ("seqlens_k_host", _ip), ("num_splits", _i),
+                ("workspace", _vp), ("workspace_bytes", _sz), ("alibi_slopes", _vp)]
+
+
 _SIGS = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp]),
     "fa_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _ip,
@@ -30,6 +48,8 @@ _SIGS = {
     "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _ip, _i]),
     "fa_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _ip, _i, _vp,
                              _sz, _vp]),
+    "fa_fwd_ex": (_i, [ctypes.POINTER(FwdArgs), _vp]),
+    "fa_decode_ex": (_i, [ctypes.POINTER(DecodeArgs), _vp]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
@@ -90,6 +110,31 @@ def _host_ints(x) -> Optional[ctypes.Array]:
     return (ctypes.c_int * len(vals))(*vals)
 
 
+def alibi_slopes(num_heads: int) -> list:
+    """The geometric ALiBi slope schedule of Press et al. (ALiBi paper): for n heads, n a power
+    of two, slopes 2^(-8/n), 2^(-16/n), ..., 2^(-8); otherwise the schedule of the largest power
+    of two below n followed by every other slope of the schedule for twice that power.  The
+    source pages give no slopes; this is the usual choice, offered for convenience."""
+    def pow2(n):
+        return [2.0 ** (-8.0 * (i + 1) / n) for i in range(n)]
+    if num_heads <= 0:
+        return []
+    p2 = 1 << (num_heads.bit_length() - 1)
+    if p2 == num_heads:
+        return pow2(num_heads)
+    return pow2(p2) + pow2(2 * p2)[0::2][: num_heads - p2]
+
+
+def _slopes_ptr(alibi_slopes, Hq: int, device):
+    if alibi_slopes is None:
+        return None, None
+    t = alibi_slopes if isinstance(alibi_slopes, torch.Tensor) else torch.tensor(alibi_slopes, dtype=torch.float32)
+    t = t.to(device=device, dtype=torch.float32).contiguous()
+    if t.numel() != Hq:
+        raise FAError(FA_ERR_INVALID, "alibi_slopes needs one slope per query head")
+    return t, t.data_ptr()
+
+
 def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
     if isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous():
         return
@@ -103,9 +148,10 @@ def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, window: int = 0,
            scale: Optional[float] = None, seqlens_q: Optional[torch.Tensor] = None,
            seqlens_k: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-           lse: Optional[torch.Tensor] = None, return_lse: bool = True
+           lse: Optional[torch.Tensor] = None, return_lse: bool = True, alibi_slopes=None
            ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Padded-batch prefill.  q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d] bf16 -> (O, LSE [B, Hq, Nq])."""
+    """Padded-batch prefill.  q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d] bf16 -> (O, LSE [B, Hq, Nq]).
+    alibi_slopes: optional per-query-head slopes (bias -m_h |p - j| on the scaled scores)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)
@@ -122,8 +168,15 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
-    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, sc,
-                      int(bool(causal)), int(window), _ptr(seqlens_q), _ptr(seqlens_k), _stream(q)))
+    if alibi_slopes is None:
+        _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, sc,
+                          int(bool(causal)), int(window), _ptr(seqlens_q), _ptr(seqlens_k), _stream(q)))
+        return o, lse
+    keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
+    a = FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
+                scale=sc, causal=int(bool(causal)), window=int(window), seqlens_q=_ptr(seqlens_q),
+                seqlens_k=_ptr(seqlens_k), alibi_slopes=sp)
+    _check(lib.fa_fwd_ex(ctypes.byref(a), _stream(q)))
     return o, lse
 
 
@@ -131,7 +184,7 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                   cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
                   window: int = 0, scale: Optional[float] = None, cu_seqlens_q_host: Optional[Sequence[int]] = None,
                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                  return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                  return_lse: bool = True, alibi_slopes=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Packed varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] -> (O, LSE [Hq, total_q])."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -150,6 +203,15 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
     host = _host_ints(cu_seqlens_q_host)
+    if alibi_slopes is not None:
+        keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
+        a = FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv,
+                    Nq=int(max_seqlen_q), Nk=int(max_seqlen_k), d=d, scale=sc, causal=int(bool(causal)),
+                    window=int(window), cu_seqlens_q=_ptr(cu_seqlens_q), cu_seqlens_k=_ptr(cu_seqlens_k),
+                    total_q=total_q, total_k=total_k,
+                    cu_seqlens_q_host=ctypes.cast(host, _ip) if host is not None else None, alibi_slopes=sp)
+        _check(lib.fa_fwd_ex(ctypes.byref(a), _stream(q)))
+        return o, lse
     _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, total_q, total_k,
                              int(max_seqlen_q), int(max_seqlen_k), d, sc, int(bool(causal)), int(window),
                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
@@ -172,7 +234,7 @@ def fa_decode_max_splits(B: int, Hq: int, Hkv: int, Ncap: int, window: int = 0, 
 def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seqlens_k: torch.Tensor,
               window: int = 0, scale: Optional[float] = None, num_splits: int = 0, seqlens_k_host=None,
               workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-              lse: Optional[torch.Tensor] = None, return_lse: bool = True
+              lse: Optional[torch.Tensor] = None, return_lse: bool = True, alibi_slopes=None
               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Decode: q [B, Hq, d], caches [B, Ncap, Hkv, d], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
     lib = load_library()
@@ -194,9 +256,17 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     if return_lse and lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
-    _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
-                         int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(q)))
+    if alibi_slopes is None:
+        _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
+                             int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(q)))
+        return o, lse
+    keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
+    a = DecodeArgs(q=_ptr(q), k=_ptr(k_cache), v=_ptr(v_cache), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv, d=d,
+                   scale=sc, window=int(window), Ncap=Ncap, seqlens_k=_ptr(seqlens_k), seqlens_k_host=hostp,
+                   num_splits=int(num_splits), workspace=_ptr(workspace),
+                   workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp)
+    _check(lib.fa_decode_ex(ctypes.byref(a), _stream(q)))
     return o, lse
 
 
@@ -204,7 +274,7 @@ def fa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
                     seqlens_k: torch.Tensor, window: int = 0, scale: Optional[float] = None, num_splits: int = 0,
                     seqlens_k_host=None, workspace: Optional[torch.Tensor] = None,
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                    return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                    return_lse: bool = True, alibi_slopes=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Decode over a paged cache: q [B, Hq, d], pages [num_pages, page_size, Hkv, d],
     block_table int32 [B, max_blocks], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
     lib = load_library()
@@ -229,6 +299,15 @@ def fa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
     if return_lse and lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    if alibi_slopes is not None:
+        keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
+        a = DecodeArgs(q=_ptr(q), k=_ptr(k_pages), v=_ptr(v_pages), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv,
+                       d=d, scale=sc, window=int(window), block_table=_ptr(block_table), max_blocks=max_blocks,
+                       page_size=page_size, num_pages=num_pages, seqlens_k=_ptr(seqlens_k), seqlens_k_host=hostp,
+                       num_splits=int(num_splits), workspace=_ptr(workspace),
+                       workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp)
+        _check(lib.fa_decode_ex(ctypes.byref(a), _stream(q)))
+        return o, lse
     _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(o), _ptr(lse), B, Hq, Hkv, num_pages,
                                page_size, d, sc, int(window), _ptr(block_table), max_blocks, _ptr(seqlens_k), hostp,
                                int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),

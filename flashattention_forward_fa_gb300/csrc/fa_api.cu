@@ -161,96 +161,126 @@ extern "C" {
 
 const char* fa_last_error(void) { return g_last_error.c_str(); }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                 int Nk, int d, float scale, int causal, int window, const int* seqlens_q, const int* seqlens_k,
-                 fa_stream_t stream) {
-  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, d, scale);
+fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
+  if (!a) return fail(FA_ERR_INVALID, "args must be non-null");
+  const int B = a->B, Hq = a->Hq, Hkv = a->Hkv, d = a->d, window = a->window;
+  fa_status st = check_common(a->q, a->k, a->v, a->o, a->lse, B, Hq, Hkv, d, a->scale);
   if (st != FA_OK) return st;
-  if (Nq <= 0 || Nk <= 0) return fail(FA_ERR_INVALID, "Nq and Nk must be positive");
-  if ((long long)B * Nq >= (1LL << 31) || (long long)B * Nk >= (1LL << 31))
-    return fail(FA_ERR_INVALID, "B * N must be below 2^31 rows");
-  if ((long long)Nq + Nk + (window > 0 ? window : 0) >= (1LL << 30))
-    return fail(FA_ERR_INVALID, "sequence lengths too large");
+  if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u))
+    return fail(FA_ERR_INVALID, "alibi_slopes must be 4-byte aligned");
+  const bool packed = a->cu_seqlens_q || a->cu_seqlens_k;
+  long long q_rows, k_rows;
+  int max_rows;
+  if (packed) {
+    if (!a->cu_seqlens_q || !a->cu_seqlens_k) return fail(FA_ERR_INVALID, "cu_seqlens_q/k must be non-null");
+    if (a->total_q < 0 || a->total_k < 0 || a->Nq < 0 || a->Nk < 0)
+      return fail(FA_ERR_INVALID, "totals and max lengths must be >= 0");
+    if ((long long)a->Nq + a->Nk + (window > 0 ? window : 0) >= (1LL << 30))
+      return fail(FA_ERR_INVALID, "sequence lengths too large");
+    if (const int* cu = a->cu_seqlens_q_host) {
+      if (cu[0] != 0) return fail(FA_ERR_INVALID, "cu_seqlens_q[0] must be 0");
+      for (int b = 0; b < B; ++b) {
+        const int len = cu[b + 1] - cu[b];
+        if (len < 0) return fail(FA_ERR_INVALID, "cu_seqlens_q must be non-decreasing (at %d)", b);
+        if (len > a->Nq) return fail(FA_ERR_INVALID, "sequence %d longer than max_seqlen_q", b);
+      }
+      if (cu[B] != a->total_q) return fail(FA_ERR_INVALID, "cu_seqlens_q[B] != total_q");
+    }
+    if (a->total_q == 0 || a->Nq == 0) return FA_OK;  // nothing to compute
+    q_rows = a->total_q;
+    k_rows = a->total_k > 0 ? a->total_k : 1;  // a map needs one row; no key row is read when total_k = 0
+    max_rows = a->Nq;
+  } else {
+    if (a->Nq <= 0 || a->Nk <= 0) return fail(FA_ERR_INVALID, "Nq and Nk must be positive");
+    if ((long long)B * a->Nq >= (1LL << 31) || (long long)B * a->Nk >= (1LL << 31))
+      return fail(FA_ERR_INVALID, "B * N must be below 2^31 rows");
+    if ((long long)a->Nq + a->Nk + (window > 0 ? window : 0) >= (1LL << 30))
+      return fail(FA_ERR_INVALID, "sequence lengths too large");
+    q_rows = (long long)B * a->Nq;
+    k_rows = (long long)B * a->Nk;
+    max_rows = a->Nq;
+  }
+  if (B > 65535) return fail(FA_ERR_INVALID, "grid too large");
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   if ((st = get_encoder()) != FA_OK) return st;
   const int bm = fa::prefill_box_rows();
   CUtensorMap tq, tk, tv;
-  if ((st = make_map(&tq, q, d, Hq, (long long)B * Nq, bm, "q")) != FA_OK) return st;
-  if ((st = make_map(&tk, k, d, Hkv, (long long)B * Nk, 128, "k")) != FA_OK) return st;
-  if ((st = make_map(&tv, v, d, Hkv, (long long)B * Nk, 128, "v")) != FA_OK) return st;
+  if ((st = make_map(&tq, a->q, d, Hq, q_rows, bm, "q")) != FA_OK) return st;
+  if ((st = make_map(&tk, a->k, d, Hkv, k_rows, 128, "k")) != FA_OK) return st;
+  if ((st = make_map(&tv, a->v, d, Hkv, k_rows, 128, "v")) != FA_OK) return st;
   fa::PrefillParams p{};
-  p.o = o;
-  p.lse = lse;
-  p.cu_q = p.cu_k = nullptr;
-  p.seqlens_q = seqlens_q;
-  p.seqlens_k = seqlens_k;
+  p.o = a->o;
+  p.lse = a->lse;
+  p.cu_q = packed ? a->cu_seqlens_q : nullptr;
+  p.cu_k = packed ? a->cu_seqlens_k : nullptr;
+  p.seqlens_q = packed ? nullptr : a->seqlens_q;
+  p.seqlens_k = packed ? nullptr : a->seqlens_k;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.Nq = Nq;
-  p.Nk = Nk;
+  p.Nq = a->Nq;
+  p.Nk = a->Nk;
   p.group = Hq / Hkv;
-  p.scale_log2 = scale * kLog2e;
-  p.causal = causal ? 1 : 0;
+  p.scale_log2 = a->scale * kLog2e;
+  p.causal = a->causal ? 1 : 0;
   p.window = window > 0 ? window : 0;
   p.err = di->status;
-  if (B > 65535) return fail(FA_ERR_INVALID, "grid too large");
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, Nq, reinterpret_cast<cudaStream_t>(stream));
+  p.alibi = a->alibi_slopes;
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_rows, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                 int Nk, int d, float scale, int causal, int window, const int* seqlens_q, const int* seqlens_k,
+                 fa_stream_t stream) {
+  fa_fwd_args a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.window = window;
+  a.seqlens_q = seqlens_q;
+  a.seqlens_k = seqlens_k;
+  return fa_fwd_ex(&a, stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d, float scale,
                         int causal, int window, const int* cu_seqlens_q, const int* cu_seqlens_k,
                         const int* cu_seqlens_q_host, fa_stream_t stream) {
-  fa_status st = check_common(q, k, v, o, lse, B, Hq, Hkv, d, scale);
-  if (st != FA_OK) return st;
   if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID, "cu_seqlens_q/k must be non-null");
-  if (total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
-    return fail(FA_ERR_INVALID, "totals and max lengths must be >= 0");
-  if ((long long)max_seqlen_q + max_seqlen_k + (window > 0 ? window : 0) >= (1LL << 30))
-    return fail(FA_ERR_INVALID, "sequence lengths too large");
-  if (cu_seqlens_q_host) {
-    if (cu_seqlens_q_host[0] != 0) return fail(FA_ERR_INVALID, "cu_seqlens_q[0] must be 0");
-    for (int b = 0; b < B; ++b) {
-      const int len = cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b];
-      if (len < 0) return fail(FA_ERR_INVALID, "cu_seqlens_q must be non-decreasing (at %d)", b);
-      if (len > max_seqlen_q) return fail(FA_ERR_INVALID, "sequence %d longer than max_seqlen_q", b);
-    }
-    if (cu_seqlens_q_host[B] != total_q) return fail(FA_ERR_INVALID, "cu_seqlens_q[B] != total_q");
-  }
-  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;  // nothing to compute
-  DeviceInfo* di = nullptr;
-  if ((st = device_info(&di)) != FA_OK) return st;
-  if ((st = get_encoder()) != FA_OK) return st;
-  const int bm = fa::prefill_box_rows();
-  CUtensorMap tq, tk, tv;
-  const long long kr = total_k > 0 ? total_k : 1;  // a map needs one row; no key row is read when total_k = 0
-  if ((st = make_map(&tq, q, d, Hq, total_q, bm, "q")) != FA_OK) return st;
-  if ((st = make_map(&tk, k, d, Hkv, kr, 128, "k")) != FA_OK) return st;
-  if ((st = make_map(&tv, v, d, Hkv, kr, 128, "v")) != FA_OK) return st;
-  fa::PrefillParams p{};
-  p.o = o;
-  p.lse = lse;
-  p.cu_q = cu_seqlens_q;
-  p.cu_k = cu_seqlens_k;
-  p.seqlens_q = p.seqlens_k = nullptr;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Nq = max_seqlen_q;
-  p.Nk = max_seqlen_k;
-  p.group = Hq / Hkv;
-  p.scale_log2 = scale * kLog2e;
-  p.causal = causal ? 1 : 0;
-  p.window = window > 0 ? window : 0;
-  p.err = di->status;
-  if (B > 65535) return fail(FA_ERR_INVALID, "grid too large");
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_seqlen_q, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "prefill (varlen) launch");
-  return FA_OK;
+  fa_fwd_args a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = max_seqlen_q;
+  a.Nk = max_seqlen_k;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal;
+  a.window = window;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.cu_seqlens_q_host = cu_seqlens_q_host;
+  return fa_fwd_ex(&a, stream);
 }
 
 size_t fa_decode_workspace_size(int B, int Hq, int d, int max_splits) {
@@ -314,90 +344,57 @@ int fa_decode_max_splits(int B, int Hq, int Hkv, int Ncap, int window, const int
   return plan_decode(B, Hkv, Hq / Hkv, Ncap, window, seqlens_k_host, num_splits, sm).max_splits;
 }
 
-fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
-                    int Hkv, int Ncap, int d, float scale, int window, const int* seqlens_k,
-                    const int* seqlens_k_host, int num_splits, void* workspace, size_t workspace_bytes,
-                    fa_stream_t stream) {
-  fa_status st = check_common(q, k_cache, v_cache, o, lse, B, Hq, Hkv, d, scale);
+fa_status fa_decode_ex(const fa_decode_args* a, fa_stream_t stream) {
+  if (!a) return fail(FA_ERR_INVALID, "args must be non-null");
+  const int B = a->B, Hq = a->Hq, Hkv = a->Hkv, d = a->d, window = a->window;
+  fa_status st = check_common(a->q, a->k, a->v, a->o, a->lse, B, Hq, Hkv, d, a->scale);
   if (st != FA_OK) return st;
-  if (Ncap <= 0) return fail(FA_ERR_INVALID, "Ncap must be positive");
-  if (!seqlens_k) return fail(FA_ERR_INVALID, "seqlens_k must be non-null");
-  if (num_splits < 0) return fail(FA_ERR_INVALID, "num_splits must be >= 0");
-  if ((long long)B * Ncap >= (1LL << 31)) return fail(FA_ERR_INVALID, "B * Ncap must be below 2^31 rows");
+  if (!a->seqlens_k) return fail(FA_ERR_INVALID, "seqlens_k must be non-null");
+  if (a->num_splits < 0) return fail(FA_ERR_INVALID, "num_splits must be >= 0");
+  if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u))
+    return fail(FA_ERR_INVALID, "alibi_slopes must be 4-byte aligned");
   if (B > 65535) return fail(FA_ERR_INVALID, "B too large");
+  const bool paged = a->block_table != nullptr;
+  long long rows;  // rows of the K/V tensors as TMA sees them
+  int cap;         // keys a sequence can hold
+  if (paged) {
+    if (a->page_size <= 0 || a->page_size % 64 != 0)
+      return fail(FA_ERR_INVALID, "page_size (%d) must be a positive multiple of 64", a->page_size);
+    if (a->num_pages <= 0 || a->max_blocks <= 0)
+      return fail(FA_ERR_INVALID, "num_pages and max_blocks must be positive");
+    if ((long long)a->num_pages * a->page_size >= (1LL << 31) || (long long)a->max_blocks * a->page_size >= (1LL << 30))
+      return fail(FA_ERR_INVALID, "paged cache too large");
+    rows = (long long)a->num_pages * a->page_size;
+    cap = a->max_blocks * a->page_size;
+  } else {
+    if (a->Ncap <= 0) return fail(FA_ERR_INVALID, "Ncap must be positive");
+    if ((long long)B * a->Ncap >= (1LL << 31)) return fail(FA_ERR_INVALID, "B * Ncap must be below 2^31 rows");
+    rows = (long long)B * a->Ncap;
+    cap = a->Ncap;
+  }
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
-  const DecodePlan pl = plan_decode(B, Hkv, Hq / Hkv, Ncap, window, seqlens_k_host, num_splits, di->sm_count);
+  // paged chunks start on a 64-key boundary at or below the window start: plan with window + 63
+  const int plan_window = (paged && window > 0) ? window + 63 : window;
+  const DecodePlan pl =
+      plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, a->seqlens_k_host, a->num_splits, di->sm_count);
   const size_t need = fa_decode_workspace_size(B, Hq, d, pl.max_splits);
-  if (!workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
-  if (!aligned16(workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
-  if (workspace_bytes < need)
-    return fail(FA_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (!a->workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
+  if (!aligned16(a->workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
+  if (a->workspace_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", a->workspace_bytes, need);
   if (pl.max_splits > 65535) return fail(FA_ERR_INVALID, "too many splits");
   if ((st = get_encoder()) != FA_OK) return st;
   CUtensorMap tk, tv;
   const int bn = fa::decode_block_n();
-  if ((st = make_map(&tk, k_cache, d, Hkv, (long long)B * Ncap, bn, "k_cache")) != FA_OK) return st;
-  if ((st = make_map(&tv, v_cache, d, Hkv, (long long)B * Ncap, bn, "v_cache")) != FA_OK) return st;
+  if ((st = make_map(&tk, a->k, d, Hkv, rows, bn, "k cache")) != FA_OK) return st;
+  if ((st = make_map(&tv, a->v, d, Hkv, rows, bn, "v cache")) != FA_OK) return st;
   fa::DecodeParams p{};
-  p.q = q;
-  p.o = o;
-  p.lse = lse;
-  p.seqlens_k = seqlens_k;
-  p.o_part = static_cast<float*>(workspace);
-  p.lse_part = p.o_part + (size_t)B * Hq * pl.max_splits * d;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Ncap = Ncap;
-  p.group = Hq / Hkv;
-  p.chunk = pl.chunk;
-  p.max_splits = pl.max_splits;
-  p.window = window > 0 ? window : 0;
-  p.scale_log2 = scale * kLog2e;
-  p.err = di->status;
-  cudaError_t e = fa::launch_decode(d, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  return FA_OK;
-}
-
-fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, float* lse, int B,
-                          int Hq, int Hkv, int num_pages, int page_size, int d, float scale, int window,
-                          const int* block_table, int max_blocks, const int* seqlens_k, const int* seqlens_k_host,
-                          int num_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  fa_status st = check_common(q, k_pages, v_pages, o, lse, B, Hq, Hkv, d, scale);
-  if (st != FA_OK) return st;
-  if (!seqlens_k || !block_table) return fail(FA_ERR_INVALID, "seqlens_k and block_table must be non-null");
-  if (page_size <= 0 || page_size % 64 != 0)
-    return fail(FA_ERR_INVALID, "page_size (%d) must be a positive multiple of 64", page_size);
-  if (num_pages <= 0 || max_blocks <= 0) return fail(FA_ERR_INVALID, "num_pages and max_blocks must be positive");
-  if ((long long)num_pages * page_size >= (1LL << 31) || (long long)max_blocks * page_size >= (1LL << 30))
-    return fail(FA_ERR_INVALID, "paged cache too large");
-  if (num_splits < 0) return fail(FA_ERR_INVALID, "num_splits must be >= 0");
-  if (B > 65535) return fail(FA_ERR_INVALID, "B too large");
-  DeviceInfo* di = nullptr;
-  if ((st = device_info(&di)) != FA_OK) return st;
-  const int cap = max_blocks * page_size;
-  // chunks start on a 64-key boundary at or below the window start: plan with window + 63
-  const int plan_window = window > 0 ? window + 63 : 0;
-  const DecodePlan pl = plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, seqlens_k_host, num_splits, di->sm_count);
-  const size_t need = fa_decode_workspace_size(B, Hq, d, pl.max_splits);
-  if (!workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
-  if (!aligned16(workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
-  if (workspace_bytes < need)
-    return fail(FA_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
-  if (pl.max_splits > 65535) return fail(FA_ERR_INVALID, "too many splits");
-  if ((st = get_encoder()) != FA_OK) return st;
-  CUtensorMap tk, tv;
-  const int bn = fa::decode_block_n();
-  if ((st = make_map(&tk, k_pages, d, Hkv, (long long)num_pages * page_size, bn, "k_pages")) != FA_OK) return st;
-  if ((st = make_map(&tv, v_pages, d, Hkv, (long long)num_pages * page_size, bn, "v_pages")) != FA_OK) return st;
-  fa::DecodeParams p{};
-  p.q = q;
-  p.o = o;
-  p.lse = lse;
-  p.seqlens_k = seqlens_k;
-  p.o_part = static_cast<float*>(workspace);
+  p.q = a->q;
+  p.o = a->o;
+  p.lse = a->lse;
+  p.seqlens_k = a->seqlens_k;
+  p.o_part = static_cast<float*>(a->workspace);
   p.lse_part = p.o_part + (size_t)B * Hq * pl.max_splits * d;
   p.B = B;
   p.Hq = Hq;
@@ -407,15 +404,72 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   p.chunk = pl.chunk;
   p.max_splits = pl.max_splits;
   p.window = window > 0 ? window : 0;
-  p.scale_log2 = scale * kLog2e;
+  p.scale_log2 = a->scale * kLog2e;
   p.err = di->status;
-  p.block_table = block_table;
-  p.max_blocks = max_blocks;
-  p.page_size = page_size;
-  p.num_pages = num_pages;
+  if (paged) {
+    p.block_table = a->block_table;
+    p.max_blocks = a->max_blocks;
+    p.page_size = a->page_size;
+    p.num_pages = a->num_pages;
+  }
+  p.alibi = a->alibi_slopes;
   cudaError_t e = fa::launch_decode(d, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return FA_OK;
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                    int Hkv, int Ncap, int d, float scale, int window, const int* seqlens_k,
+                    const int* seqlens_k_host, int num_splits, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+  fa_decode_args a{};
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.scale = scale;
+  a.window = window;
+  a.Ncap = Ncap;
+  a.seqlens_k = seqlens_k;
+  a.seqlens_k_host = seqlens_k_host;
+  a.num_splits = num_splits;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return fa_decode_ex(&a, stream);
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, float* lse, int B,
+                          int Hq, int Hkv, int num_pages, int page_size, int d, float scale, int window,
+                          const int* block_table, int max_blocks, const int* seqlens_k, const int* seqlens_k_host,
+                          int num_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!block_table) return fail(FA_ERR_INVALID, "seqlens_k and block_table must be non-null");
+  fa_decode_args a{};
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.scale = scale;
+  a.window = window;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.seqlens_k = seqlens_k;
+  a.seqlens_k_host = seqlens_k_host;
+  a.num_splits = num_splits;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return fa_decode_ex(&a, stream);
 }
 
 fa_status fa_device_status(uint32_t* bits, int clear) {

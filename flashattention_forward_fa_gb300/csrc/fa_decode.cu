@@ -101,7 +101,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool ALIBI>
 __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecodeParams p) {
@@ -189,8 +189,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // With ALiBi the scale is applied together with the bias -m_h (pos - key), pos = len - 1 (the new
+  // token is the last cache slot), and everything after works on scaled scores (xs = 1).
+  const float xs = ALIBI ? 1.0f : p.scale_log2;
+  const float slope_g = (ALIBI && g < nrows) ? p.alibi[hq0 + g] * 1.4426950408889634f : 0.f;
+  const float slope_g8 = (ALIBI && g + 8 < nrows) ? p.alibi[hq0 + g + 8] * 1.4426950408889634f : 0.f;
   float lr0 = 0.f, lr1 = 0.f;  // sums of the bf16-rounded weights P V actually uses (normalise O)
-  const float sl2 = p.scale_log2;
   const uint32_t sbase = smem_u32(sm);
   bool ok = true;
 
@@ -234,13 +238,22 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
         for (int e = 0; e < 4; ++e)
           if (n * 8 + 2 * tq + (e & 1) >= nvalid || (PAGED && n * 8 + 2 * tq + (e & 1) < nlow))
             sc[n][e] = -INFINITY;
+      if (ALIBI) {
+        const float dist0 = (float)(len - 1 - (start + t * C::BN + kb + 2 * tq));  // pos - key of e = 0, n = 0
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sc[n][e] = fmaf(sc[n][e], p.scale_log2,
+                            -(e < 2 ? slope_g : slope_g8) * (dist0 - (float)(n * 8 + (e & 1))));
+      }
       float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0 * sl2), mn1 = fmaxf(m1, mx1 * sl2);
+      const float mn0 = fmaxf(m0, mx0 * xs), mn1 = fmaxf(m1, mx1 * xs);
       if (mn0 > m0 + 8.0f) {  // lazy rescale: the exponent base moves only on large jumps
         const float a = ex2_approx(m0 - mn0);
         l0 *= a;
@@ -261,10 +274,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       float pe[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
-        pe[n][0] = ex2_approx(fmaf(sc[n][0], sl2, -mu0));
-        pe[n][1] = ex2_approx(fmaf(sc[n][1], sl2, -mu0));
-        pe[n][2] = ex2_approx(fmaf(sc[n][2], sl2, -mu1));
-        pe[n][3] = ex2_approx(fmaf(sc[n][3], sl2, -mu1));
+        pe[n][0] = ex2_approx(fmaf(sc[n][0], xs, -mu0));
+        pe[n][1] = ex2_approx(fmaf(sc[n][1], xs, -mu0));
+        pe[n][2] = ex2_approx(fmaf(sc[n][2], xs, -mu1));
+        pe[n][3] = ex2_approx(fmaf(sc[n][3], xs, -mu1));
         l0 += pe[n][0] + pe[n][1];
         l1 += pe[n][2] + pe[n][3];
       }
@@ -400,7 +413,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = mx + __logf(tot);
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool ALIBI>
 static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                                    cudaStream_t stream) {
   using C = DecodeCfg<D>;
@@ -410,14 +423,14 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_decode_split_kernel<D, PAGED, ALIBI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   const int n_rb = (p.group + 15) / 16;
   dim3 grid(p.max_splits, p.Hkv * n_rb, p.B);
-  fa_decode_split_kernel<D, PAGED><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
+  fa_decode_split_kernel<D, PAGED, ALIBI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = p.B * p.Hq;
@@ -425,11 +438,18 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_decode_dd(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                                    cudaStream_t stream) {
+  const bool paged = p.page_size > 0, alibi = p.alibi != nullptr;
+  if (paged) return alibi ? launch_decode_d<D, true, true>(tk, tv, p, stream)
+                          : launch_decode_d<D, true, false>(tk, tv, p, stream);
+  return alibi ? launch_decode_d<D, false, true>(tk, tv, p, stream) : launch_decode_d<D, false, false>(tk, tv, p, stream);
+}
+
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           cudaStream_t stream) {
-  const bool paged = p.page_size > 0;
-  if (d == 64) return paged ? launch_decode_d<64, true>(tk, tv, p, stream) : launch_decode_d<64, false>(tk, tv, p, stream);
-  return paged ? launch_decode_d<128, true>(tk, tv, p, stream) : launch_decode_d<128, false>(tk, tv, p, stream);
+  return d == 64 ? launch_decode_dd<64>(tk, tv, p, stream) : launch_decode_dd<128>(tk, tv, p, stream);
 }
 
 int decode_block_n() { return DecodeCfg<128>::BN; }

@@ -19,6 +19,7 @@ struct PrefillParams {
   float scale_log2;        // scale * log2(e)
   int causal, window;
   uint32_t* err;           // device status word
+  const float* alibi;      // per-query-head ALiBi slopes (fp32 [Hq]) or nullptr
 };
 
 struct DecodeParams {
@@ -38,6 +39,7 @@ struct DecodeParams {
   // lives in page block_table[b * max_blocks + j / page_size]; page_size is a multiple of 64.
   const int* block_table;
   int max_blocks, page_size, num_pages;
+  const float* alibi;      // per-query-head ALiBi slopes (fp32 [Hq]) or nullptr
 };
 
 // max_rows: rows per sequence (padded layout) or the longest sequence (packed layout).

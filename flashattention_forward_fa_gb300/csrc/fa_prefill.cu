@@ -26,6 +26,9 @@
 //   means O_X already holds PV_X(t): the softmax may rescale O_X without a wait.
 //   The rescale is lazy: the exponent base only moves when a tile's max exceeds
 //   it by more than 2^8; the final O / l uses the same base, so it is exact.
+//   With ALiBi (jsqmd page, §三 "ALiBi位置编码的线性偏置") each score gets
+//   -m_h |p - j| (p the query's absolute position) right after masking, folded into
+//   the same fused multiply-add that applies the softmax scale.
 //   Each Q tile visits only the K/V tiles its rows can see (causal / window
 //   tiles that are fully masked are never loaded or multiplied); only tiles
 //   crossing a mask edge or the ragged tail evaluate the mask.
@@ -171,7 +174,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D>
+template <int D, bool ALIBI>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -256,7 +259,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     visible_keys(pos, s.Lk, p.causal, p.window, row_lo, row_hi);
     const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t colS = C::COL_S + 128u * X, colO = C::COL_O + (uint32_t)D * X;
+    // scores are scaled into log2 units by sl2; with ALiBi the scale is applied together with
+    // the bias below and everything after works on already-scaled scores (xs = 1)
     const float sl2 = p.scale_log2;
+    const float xs = ALIBI ? 1.0f : sl2;
+    const float slope2 = ALIBI ? p.alibi[h] * 1.4426950408889634f : 0.f;  // m_h in log2 units
     float m = -INFINITY;  // running max used for exponentiation (log2 units)
     float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
     float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
@@ -297,6 +304,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         for (int j = 0; j < C::BN; ++j)
           if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
       }
+      if (ALIBI) {
+        const float dpos = (float)(pos - k0);
+#pragma unroll
+        for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
+      }
       float mx;
       {  // row max: eight independent chains of three-input max
         float t8[8];
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
         mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
       }
-      mx *= sl2;
+      mx *= xs;
       const float m_new = fmaxf(m, mx);
       const bool need = m_new > m + 8.0f;  // -inf + 8 = -inf: the first finite max always moves m
       const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
       // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
       // (two accumulators each to keep the dependency chains short).
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
+      const uint64_t sl2x2 = f2_pack(xs, xs), negm2 = f2_pack(-m_use, -m_use);
       uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       float lr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool ALIBI>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, int max_rows, cudaStream_t stream) {
   using C = PrefillCfg<D>;
@@ -544,21 +556,25 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   const int rows_per_cta = C::NQT * C::BM;
   dim3 grid(p.Hq, (max_rows + rows_per_cta - 1) / rows_per_cta, p.B);
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-  fa_prefill_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  fa_prefill_kernel<D, ALIBI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int max_rows, cudaStream_t stream) {
-  if (d == 64) return launch_prefill_d<64>(tq, tk, tv, p, max_rows, stream);
-  return launch_prefill_d<128>(tq, tk, tv, p, max_rows, stream);
+  if (p.alibi)
+    return d == 64 ? launch_prefill_d<64, true>(tq, tk, tv, p, max_rows, stream)
+                   : launch_prefill_d<128, true>(tq, tk, tv, p, max_rows, stream);
+  return d == 64 ? launch_prefill_d<64, false>(tq, tk, tv, p, max_rows, stream)
+                 : launch_prefill_d<128, false>(tq, tk, tv, p, max_rows, stream);
 }
 
 int prefill_box_rows() { return PrefillCfg<128>::BM; }

@@ -103,6 +103,37 @@ FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void
                         fa_stream_t stream);
 
 /*
+ * All prefill options in one call (the entry points above are special cases).
+ * Layout: packed when cu_seqlens_q and cu_seqlens_k are both set (as
+ * fa_fwd_varlen: Nq/Nk are then the maximum lengths, total_q/total_k the row
+ * counts, cu_seqlens_q_host optional), else padded (as fa_fwd, with optional
+ * seqlens_q/seqlens_k).
+ * alibi_slopes: NULL, or device fp32 [Hq]: ALiBi (jsqmd page, §三 "ALiBi位置编码的
+ *   线性偏置") adds -alibi_slopes[h] * |p - j| to every scaled score, p the
+ *   query's absolute position (i + Lk - Lq, the causal alignment).  The pages
+ *   give no slope values; the caller chooses them.
+ */
+typedef struct fa_fwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk, d;
+  float scale;
+  int causal, window;
+  const int* seqlens_q;          /* padded layout (optional) */
+  const int* seqlens_k;
+  const int* cu_seqlens_q;       /* packed layout */
+  const int* cu_seqlens_k;
+  int total_q, total_k;
+  const int* cu_seqlens_q_host;  /* packed layout, optional host copy for checking */
+  const float* alibi_slopes;     /* optional */
+} fa_fwd_args;
+
+FA_API fa_status fa_fwd_ex(const fa_fwd_args* args, fa_stream_t stream);
+
+/*
  * Bytes of fp32 workspace fa_decode needs for a given split bound
  * (partial outputs [B, Hq, max_splits, d] and partial LSE [B, Hq, max_splits]).
  */
@@ -151,6 +182,35 @@ FA_API fa_status fa_decode_paged(const void* q, const void* k_pages, const void*
                                  const int* seqlens_k, const int* seqlens_k_host,
                                  int num_splits, void* workspace, size_t workspace_bytes,
                                  fa_stream_t stream);
+
+/*
+ * All decode options in one call (fa_decode and fa_decode_paged are special
+ * cases).  The cache is paged when block_table is set (as fa_decode_paged: k/v
+ * are the page pools, num_pages/page_size/max_blocks describe them), else
+ * contiguous [B, Ncap, Hkv, d] (as fa_decode).  alibi_slopes as in fa_fwd_args:
+ * the new token sits at position len - 1, so key j gets -m_h * (len - 1 - j).
+ */
+typedef struct fa_decode_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, d;
+  float scale;
+  int window;
+  int Ncap;                      /* contiguous cache */
+  const int* block_table;        /* paged cache (optional) */
+  int max_blocks, page_size, num_pages;
+  const int* seqlens_k;
+  const int* seqlens_k_host;     /* optional */
+  int num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  const float* alibi_slopes;     /* optional */
+} fa_decode_args;
+
+FA_API fa_status fa_decode_ex(const fa_decode_args* args, fa_stream_t stream);
 
 /*
  * The split bound S that fa_decode uses for the same arguments on the current

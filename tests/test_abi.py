@@ -156,3 +156,32 @@ def test_paged_decode_arguments_checked(lib):
     assert L.fa_decode_paged(*args(lens=None)) == 1
     assert L.fa_decode_paged(*args(num_pages=0)) == 1
     assert L.fa_decode_paged(*args(max_blocks=0)) == 1
+
+
+def test_ex_entry_points_read_their_structs(lib):
+    # the ctypes mirrors of fa_fwd_args / fa_decode_args line up with the C layout: each field
+    # checked here is read from its own offset and triggers its own host-side error
+    _, b = _binding()
+    L = b.load_library()
+    d = 0x1000
+    a = b.FwdArgs(q=d, k=d, v=d, o=d, B=1, Hq=6, Hkv=4, Nq=8, Nk=8, d=64, scale=0.1)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"multiple" in L.fa_last_error()
+    a = b.FwdArgs(q=d, k=d, v=d, o=d, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=96, scale=0.1)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 2
+    a = b.FwdArgs(q=d, k=d, v=d, o=d, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=64, scale=0.1, alibi_slopes=0x1002)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"alibi" in L.fa_last_error()
+    a = b.FwdArgs(q=d, k=d, v=d, o=d, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=64, scale=0.1, cu_seqlens_q=d)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"cu_seqlens" in L.fa_last_error()
+    x = b.DecodeArgs(q=d, k=d, v=d, o=d, B=2, Hq=8, Hkv=2, d=128, scale=0.1, Ncap=64, seqlens_k=d,
+                     block_table=d, page_size=96, num_pages=4, max_blocks=2)
+    assert L.fa_decode_ex(ctypes.byref(x), None) == 1 and b"multiple of 64" in L.fa_last_error()
+    x = b.DecodeArgs(q=d, k=d, v=d, o=d, B=2, Hq=8, Hkv=2, d=128, scale=0.1, Ncap=64, num_splits=-1, seqlens_k=d)
+    assert L.fa_decode_ex(ctypes.byref(x), None) == 1 and b"num_splits" in L.fa_last_error()
+
+
+def test_alibi_slope_schedule():
+    _, b = _binding()
+    s8 = b.alibi_slopes(8)
+    assert s8 == [2.0 ** -(i + 1) for i in range(8)]
+    s12 = b.alibi_slopes(12)
+    assert s12[:8] == s8 and s12[8:] == [2.0 ** -(0.5 + i) for i in range(4)]
