@@ -454,3 +454,56 @@ def test_alibi_sign_mistake_is_caught():
     Ob, Lb = brute_force_alibi(q, k, v, 0.5, True, 0, slopes)
     Om, Lm = c_oracle_alibi(q, k, v, 0.5, True, 0, -slopes)    # planted: bias added with the wrong sign
     assert not np.allclose(Om, Ob, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+from oracle import rope as orope  # noqa: E402
+
+
+def test_rope_tables_match_math():
+    c, s = orope.tables(50, 16, base=10000.0)
+    for p in (0, 1, 7, 49):
+        for i in range(8):
+            ang = p * 10000.0 ** (-2.0 * i / 16)
+            assert abs(c[p, i] - math.cos(ang)) < 1e-15 and abs(s[p, i] - math.sin(ang)) < 1e-15
+
+
+def test_rope_rotation_against_scalar_loop():
+    x = RNG.standard_normal((6, 3, 12))
+    pos = [0, 5, 2, 9, 1, 3]
+    c, s = orope.tables(10, 8)
+    r = orope.rotate(x, pos, c, s, 8)
+    for n in range(6):
+        for h in range(3):
+            for i in range(4):
+                a, b = x[n, h, 2 * i], x[n, h, 2 * i + 1]
+                cc, ss = c[pos[n], i], s[pos[n], i]
+                assert abs(r[n, h, 2 * i] - (a * cc - b * ss)) < 1e-14
+                assert abs(r[n, h, 2 * i + 1] - (a * ss + b * cc)) < 1e-14
+            np.testing.assert_array_equal(r[n, h, 8:], x[n, h, 8:])   # past rotary_dim: unchanged
+
+
+def test_rope_position_zero_is_identity_and_norms_kept():
+    x = RNG.standard_normal((5, 2, 16))
+    c, s = orope.tables(8, 16)
+    np.testing.assert_allclose(orope.rotate(x, [0] * 5, c, s, 16), x, atol=1e-15)
+    r = orope.rotate(x, [1, 2, 3, 4, 7], c, s, 16)
+    np.testing.assert_allclose((r ** 2).sum(-1), (x ** 2).sum(-1), rtol=1e-13)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    # <R(m) q, R(n) k> is unchanged when every position moves by the same shift
+    q = RNG.standard_normal((7, 1, 16))
+    k = RNG.standard_normal((7, 1, 16))
+    c, s = orope.tables(64, 16)
+    pos = np.arange(7)
+    s0 = orope.rotate(q, pos, c, s, 16)[:, 0] @ orope.rotate(k, pos, c, s, 16)[:, 0].T
+    s1 = orope.rotate(q, pos + 40, c, s, 16)[:, 0] @ orope.rotate(k, pos + 40, c, s, 16)[:, 0].T
+    np.testing.assert_allclose(s0, s1, atol=1e-12)
+    # and a planted mistake (pairing dimension i with i + d/2 while the tables assume
+    # adjacent pairs) is not a rotation of adjacent pairs: position 1 differs
+    x = RNG.standard_normal((1, 1, 16))
+    r_adj = orope.rotate(x, [1], c, s, 16)
+    half = np.concatenate([x[..., 0::2], x[..., 1::2]], axis=-1)
+    assert not np.allclose(r_adj, orope.rotate(half, [1], c, s, 16))
