@@ -12,8 +12,10 @@ Entry points (same names as the C ABI):
 * ``fa_decode(q, k_cache, v_cache, seqlens_k, ...)``  one new token per sequence
 * ``fa_decode_paged(...)``         decode over a paged (block-table) KV cache
 * ``fa_decode_noalloc(...)``       the same decode with no device allocation at all
+* ``fa_rope(x, positions, (cos, sin))``  rotary embedding in place (K before the
+  fused prefill, or a KV cache); ``rope_tables`` builds the usual tables
 * ``fa_fwd_ex`` / ``fa_decode_ex`` (C ABI): every option in one struct; reached from
-  the wrappers above when ``alibi_slopes`` is given
+  the wrappers above when ``alibi_slopes`` or ``rope`` is given
 * ``fa_device_status()``           read/clear the kernels' error word
 """
 
@@ -32,8 +34,10 @@ from ._binding import (  # noqa: F401
     fa_device_status,
     fa_fwd,
     fa_fwd_varlen,
+    fa_rope,
     library_path,
     load_library,
+    rope_tables,
 )
 
 __all__ = [
@@ -43,6 +47,8 @@ __all__ = [
     "alibi_slopes",
     "fa_fwd",
     "fa_fwd_varlen",
+    "fa_rope",
+    "rope_tables",
     "fa_decode",
     "fa_decode_max_splits",
     "fa_decode_noalloc",

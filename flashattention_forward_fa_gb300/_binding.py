@@ -27,7 +27,8 @@ class FwdArgs(ctypes.Structure):
                 ("B", _i), ("Hq", _i), ("Hkv", _i), ("Nq", _i), ("Nk", _i), ("d", _i),
                 ("scale", _f), ("causal", _i), ("window", _i),
                 ("seqlens_q", _vp), ("seqlens_k", _vp), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
-                ("total_q", _i), ("total_k", _i), ("cu_seqlens_q_host", _ip), ("alibi_slopes", _vp)]
+                ("total_q", _i), ("total_k", _i), ("cu_seqlens_q_host", _ip), ("alibi_slopes", _vp),
+                ("rope_cos", _vp), ("rope_sin", _vp), ("rope_rows", _i), ("rope_dim", _i)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -51,6 +52,7 @@ _SIGS = {
     "fa_fwd_ex": (_i, [ctypes.POINTER(FwdArgs), _vp]),
     "fa_decode_ex": (_i, [ctypes.POINTER(DecodeArgs), _vp]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
+    "fa_rope": (_i, [_vp, ctypes.c_longlong, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
 }
@@ -145,13 +147,64 @@ def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16):
     raise FAError(FA_ERR_INVALID, f"{name} must be contiguous")
 
 
+def rope_tables(max_pos: int, rotary_dim: int, base: float = 10000.0, device="cuda"):
+    """The usual RoPE tables: angle p * base^(-2i / rotary_dim) for position p < max_pos and pair
+    i < rotary_dim / 2, as fp32 (cos, sin) tensors [max_pos, rotary_dim / 2] on `device`.  A setup
+    step run once per model (the tables are an input of fa_rope and of the fused prefill)."""
+    i = torch.arange(rotary_dim // 2, dtype=torch.float64)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * (base ** (-2.0 * i / rotary_dim))[None, :]
+    return (torch.cos(ang).to(torch.float32).contiguous().to(device),
+            torch.sin(ang).to(torch.float32).contiguous().to(device))
+
+
+def _check_tables(rope, rotary_dim: Optional[int], d: int):
+    if not (isinstance(rope, (tuple, list)) and len(rope) == 2):
+        raise FAError(FA_ERR_INVALID, "rope must be a (cos, sin) pair of tables")
+    cos_t, sin_t = rope
+    _need(cos_t, "rope cos", torch.float32)
+    _need(sin_t, "rope sin", torch.float32)
+    if cos_t.dim() != 2 or cos_t.shape != sin_t.shape:
+        raise FAError(FA_ERR_INVALID, "rope tables must both be [positions, rotary_dim / 2]")
+    rd = int(rotary_dim) if rotary_dim is not None else 2 * cos_t.shape[1]
+    if rd <= 0 or rd > d or 2 * cos_t.shape[1] != rd:
+        raise FAError(FA_ERR_INVALID, f"rope tables have {cos_t.shape[1]} pairs, rotary_dim is {rd}, d is {d}")
+    return cos_t, sin_t, rd
+
+
+def _set_rope(a: FwdArgs, rope, rotary_dim: Optional[int], d: int):
+    if rope is None:
+        return
+    cos_t, sin_t, rd = _check_tables(rope, rotary_dim, d)
+    a.rope_cos, a.rope_sin, a.rope_rows, a.rope_dim = _ptr(cos_t), _ptr(sin_t), cos_t.shape[0], rd
+
+
+def fa_rope(x: torch.Tensor, positions: torch.Tensor, rope, rotary_dim: Optional[int] = None) -> torch.Tensor:
+    """Rotate x in place: x bf16 [..., H, d], positions int32 with one entry per row of the
+    leading dims, rope = (cos, sin) tables [max_pos, rotary_dim / 2].  Returns x."""
+    lib = load_library()
+    _need(x, "x")
+    _need(positions, "positions", torch.int32)
+    if x.dim() < 2:
+        raise FAError(FA_ERR_INVALID, "x must be [..., H, d]")
+    H, d = x.shape[-2], x.shape[-1]
+    rows = x.numel() // (H * d) if x.numel() else 0
+    if positions.numel() != rows:
+        raise FAError(FA_ERR_INVALID, f"positions has {positions.numel()} entries for {rows} rows")
+    cos_t, sin_t, rd = _check_tables(rope, rotary_dim, d)
+    _check(lib.fa_rope(_ptr(x), rows, H, d, rd, _ptr(positions), _ptr(cos_t), _ptr(sin_t), cos_t.shape[0],
+                       _stream(x)))
+    return x
+
+
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False, window: int = 0,
            scale: Optional[float] = None, seqlens_q: Optional[torch.Tensor] = None,
            seqlens_k: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-           lse: Optional[torch.Tensor] = None, return_lse: bool = True, alibi_slopes=None
-           ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+           lse: Optional[torch.Tensor] = None, return_lse: bool = True, alibi_slopes=None,
+           rope=None, rotary_dim: Optional[int] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Padded-batch prefill.  q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d] bf16 -> (O, LSE [B, Hq, Nq]).
-    alibi_slopes: optional per-query-head slopes (bias -m_h |p - j| on the scaled scores)."""
+    alibi_slopes: optional per-query-head slopes (bias -m_h |p - j| on the scaled scores).
+    rope: optional (cos, sin) fp32 tables [positions, rotary_dim / 2]; the kernel rotates Q at
+    position i + Lk - Lq after loading it.  K must already be rotated (fa_rope)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)
@@ -168,7 +221,7 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
-    if alibi_slopes is None:
+    if alibi_slopes is None and rope is None:
         _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, sc,
                           int(bool(causal)), int(window), _ptr(seqlens_q), _ptr(seqlens_k), _stream(q)))
         return o, lse
@@ -176,6 +229,7 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fal
     a = FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
                 scale=sc, causal=int(bool(causal)), window=int(window), seqlens_q=_ptr(seqlens_q),
                 seqlens_k=_ptr(seqlens_k), alibi_slopes=sp)
+    _set_rope(a, rope, rotary_dim, d)
     _check(lib.fa_fwd_ex(ctypes.byref(a), _stream(q)))
     return o, lse
 
@@ -184,8 +238,10 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                   cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
                   window: int = 0, scale: Optional[float] = None, cu_seqlens_q_host: Optional[Sequence[int]] = None,
                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                  return_lse: bool = True, alibi_slopes=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Packed varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] -> (O, LSE [Hq, total_q])."""
+                  return_lse: bool = True, alibi_slopes=None, rope=None, rotary_dim: Optional[int] = None
+                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Packed varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] -> (O, LSE [Hq, total_q]).
+    alibi_slopes, rope, rotary_dim: as for fa_fwd (positions count from each sequence's start)."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)
@@ -203,13 +259,14 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
     host = _host_ints(cu_seqlens_q_host)
-    if alibi_slopes is not None:
+    if alibi_slopes is not None or rope is not None:
         keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
         a = FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv,
                     Nq=int(max_seqlen_q), Nk=int(max_seqlen_k), d=d, scale=sc, causal=int(bool(causal)),
                     window=int(window), cu_seqlens_q=_ptr(cu_seqlens_q), cu_seqlens_k=_ptr(cu_seqlens_k),
                     total_q=total_q, total_k=total_k,
                     cu_seqlens_q_host=ctypes.cast(host, _ip) if host is not None else None, alibi_slopes=sp)
+        _set_rope(a, rope, rotary_dim, d)
         _check(lib.fa_fwd_ex(ctypes.byref(a), _stream(q)))
         return o, lse
     _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, total_q, total_k,

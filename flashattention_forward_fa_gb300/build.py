@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libfa_gb300.so")
 BUILD_DIR = os.path.join(ROOT, "_build", "fa_gb300")
 
-SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu"]
+SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          f"-I{os.path.join(ROOT, 'include')}"]

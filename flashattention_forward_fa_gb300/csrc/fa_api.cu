@@ -168,6 +168,14 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
   if (st != FA_OK) return st;
   if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u))
     return fail(FA_ERR_INVALID, "alibi_slopes must be 4-byte aligned");
+  if (a->rope_cos || a->rope_sin) {
+    if (!a->rope_cos || !a->rope_sin) return fail(FA_ERR_INVALID, "rope_cos and rope_sin go together");
+    if (a->rope_dim <= 0 || a->rope_dim % 8 != 0 || a->rope_dim > d)
+      return fail(FA_ERR_INVALID, "rope_dim (%d) must be a positive multiple of 8, at most d", a->rope_dim);
+    if (a->rope_rows <= 0) return fail(FA_ERR_INVALID, "rope_rows must be positive");
+    if (!aligned16(a->rope_cos) || !aligned16(a->rope_sin))
+      return fail(FA_ERR_INVALID, "rope tables must be 16-byte aligned");
+  }
   const bool packed = a->cu_seqlens_q || a->cu_seqlens_k;
   long long q_rows, k_rows;
   int max_rows;
@@ -227,6 +235,12 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
   p.window = window > 0 ? window : 0;
   p.err = di->status;
   p.alibi = a->alibi_slopes;
+  if (a->rope_cos) {
+    p.rope_cos = a->rope_cos;
+    p.rope_sin = a->rope_sin;
+    p.rope_rows = a->rope_rows;
+    p.rope_dim = a->rope_dim;
+  }
   cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_rows, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
@@ -470,6 +484,35 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return fa_decode_ex(&a, stream);
+}
+
+fa_status fa_rope(void* x, long long rows, int heads, int d, int rotary_dim, const int* positions,
+                  const float* cos_t, const float* sin_t, int table_rows, fa_stream_t stream) {
+  if (!x || !positions || !cos_t || !sin_t) return fail(FA_ERR_INVALID, "x, positions and tables must be non-null");
+  if (rows < 0 || heads <= 0 || d <= 0 || table_rows <= 0) return fail(FA_ERR_INVALID, "bad sizes");
+  if (rotary_dim <= 0 || rotary_dim % 8 != 0 || rotary_dim > d)
+    return fail(FA_ERR_INVALID, "rotary_dim (%d) must be a positive multiple of 8, at most d", rotary_dim);
+  if (d % 8 != 0) return fail(FA_ERR_INVALID, "d must be a multiple of 8");
+  if (!aligned16(x) || !aligned16(cos_t) || !aligned16(sin_t))
+    return fail(FA_ERR_INVALID, "x and the tables must be 16-byte aligned");
+  if (rows == 0) return FA_OK;
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  fa::RopeParams p{};
+  p.x = x;
+  p.positions = positions;
+  p.cos_t = cos_t;
+  p.sin_t = sin_t;
+  p.rows = rows;
+  p.heads = heads;
+  p.d = d;
+  p.rotary_dim = rotary_dim;
+  p.table_rows = table_rows;
+  p.err = di->status;
+  cudaError_t e = fa::launch_rope(p, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+  return FA_OK;
 }
 
 fa_status fa_device_status(uint32_t* bits, int clear) {

@@ -20,7 +20,23 @@ struct PrefillParams {
   int causal, window;
   uint32_t* err;           // device status word
   const float* alibi;      // per-query-head ALiBi slopes (fp32 [Hq]) or nullptr
+  // RoPE of Q inside the kernel (rope_cos == nullptr: none): tables [rope_rows, rope_dim / 2]
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_rows, rope_dim;
 };
+
+struct RopeParams {
+  void* x;                 // bf16 [rows, heads, d], rotated in place
+  const int* positions;    // int32 [rows]
+  const float* cos_t;      // fp32 [table_rows, rotary_dim / 2]
+  const float* sin_t;
+  long long rows;
+  int heads, d, rotary_dim, table_rows;
+  uint32_t* err;
+};
+
+cudaError_t launch_rope(const RopeParams& p, int sm_count, cudaStream_t stream);
 
 struct DecodeParams {
   const void* q;           // bf16 [B, Hq, d]

@@ -29,6 +29,9 @@
 //   With ALiBi (jsqmd page, §三 "ALiBi位置编码的线性偏置") each score gets
 //   -m_h |p - j| (p the query's absolute position) right after masking, folded into
 //   the same fused multiply-add that applies the softmax scale.
+//   With RoPE (jsqmd page, §三 "融合位置编码的Attention计算") each softmax thread rotates its
+//   own Q row in shared memory right after the TMA load, before the first S_X; K arrives
+//   rotated (a K tile is read by every CTA of its head, so it is rotated once, not per CTA).
 //   Each Q tile visits only the K/V tiles its rows can see (causal / window
 //   tiles that are fully masked are never loaded or multiplied); only tiles
 //   crossing a mask edge or the ragged tail evaluate the mask.
@@ -57,8 +60,8 @@ struct PrefillCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
   // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  //           s_full[2], p_full[2], o_final[2], mma_done
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1;
+  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
@@ -174,7 +177,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D, bool ALIBI>
+template <int D, bool ALIBI, bool ROPE>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint64_t* p_full = s_full + 2;        // [2]: four warp arrivals per P of tile X
   uint64_t* o_final = p_full + 2;       // [2]: single completion, the last PV of tile X
   uint64_t* mma_done = o_final + 2;
+  uint64_t* q_ready = mma_done + 1;     // [2]: four warp arrivals once Q_X is rotated (RoPE only)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
 
@@ -236,6 +240,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       mbar_init(&o_final[i], 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(&q_ready[0], 4);
+    mbar_init(&q_ready[1], 4);
     fence_barrier_init();
   }
   if (warp == 10) {
@@ -268,7 +274,29 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
     float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
     bool ok = true;
-    for (int t = r.t0; t < r.t1; ++t) {
+    if (ROPE) {
+      // Rotate this thread's Q row (position pos) in place: 16-byte chunks of the 128-byte swizzled
+      // rows the TMA wrote, four adjacent pairs per chunk.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag, p.err));
+      if (ok && i < s.Lq) {
+        if (pos >= 0 && pos < p.rope_rows) {
+          uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
+          const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
+          const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
+          for (int c = 0; c < p.rope_dim / 8; ++c) {
+            uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
+            *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
+                               *reinterpret_cast<const float4*>(st + 4 * c));
+          }
+        } else {
+          atomicOr(p.err, kDevErrBounds);  // no table row for this position
+        }
+      }
+      fence_async_smem();  // the MMA reads Q through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[X]);
+    }
+    for (int t = r.t0; ok && t < r.t1; ++t) {
       const int n = t - r.t0;
       ok = mbar_wait(&s_full[X], n & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -493,6 +521,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (t == r.t1 - 1) umma_commit_by(leader, &o_final[X]);
     };
     bool ok = mbar_wait(bar_q, 0, abort_flag, p.err) && mbar_wait(&k_full[0], 0, abort_flag, p.err);
+    if (ROPE)  // the softmax warps rotate Q in place first
+      ok = ok && mbar_wait(&q_ready[0], 0, abort_flag, p.err) && mbar_wait(&q_ready[1], 0, abort_flag, p.err);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
@@ -546,7 +576,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool ALIBI>
+template <int D, bool ALIBI, bool ROPE>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, int max_rows, cudaStream_t stream) {
   using C = PrefillCfg<D>;
@@ -556,7 +586,7 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
@@ -564,17 +594,24 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   const int rows_per_cta = C::NQT * C::BM;
   dim3 grid(p.Hq, (max_rows + rows_per_cta - 1) / rows_per_cta, p.B);
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-  fa_prefill_kernel<D, ALIBI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  fa_prefill_kernel<D, ALIBI, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_prefill_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const PrefillParams& p, int max_rows, cudaStream_t stream) {
+  const bool alibi = p.alibi != nullptr, rope = p.rope_cos != nullptr;
+  if (alibi) return rope ? launch_prefill_d<D, true, true>(tq, tk, tv, p, max_rows, stream)
+                         : launch_prefill_d<D, true, false>(tq, tk, tv, p, max_rows, stream);
+  return rope ? launch_prefill_d<D, false, true>(tq, tk, tv, p, max_rows, stream)
+              : launch_prefill_d<D, false, false>(tq, tk, tv, p, max_rows, stream);
 }
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int max_rows, cudaStream_t stream) {
-  if (p.alibi)
-    return d == 64 ? launch_prefill_d<64, true>(tq, tk, tv, p, max_rows, stream)
-                   : launch_prefill_d<128, true>(tq, tk, tv, p, max_rows, stream);
-  return d == 64 ? launch_prefill_d<64, false>(tq, tk, tv, p, max_rows, stream)
-                 : launch_prefill_d<128, false>(tq, tk, tv, p, max_rows, stream);
+  return d == 64 ? launch_prefill_dd<64>(tq, tk, tv, p, max_rows, stream)
+                 : launch_prefill_dd<128>(tq, tk, tv, p, max_rows, stream);
 }
 
 int prefill_box_rows() { return PrefillCfg<128>::BM; }

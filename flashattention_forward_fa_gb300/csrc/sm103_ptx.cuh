@@ -299,4 +299,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// RoPE on four packed bf16 pairs: (x, y) -> (x c - y s, x s + y c) per pair, fp32 math,
+// bf16 round-to-nearest-even result (the rotation of adjacent dimension pairs).
+__device__ __forceinline__ uint32_t rope_rotate_pair(uint32_t pr, float cc, float ss) {
+  const float x = __uint_as_float(pr << 16), y = __uint_as_float(pr & 0xffff0000u);
+  return pack_bf16x2(fmaf(x, cc, -y * ss), fmaf(x, ss, y * cc));
+}
+__device__ __forceinline__ uint4 rope_rotate4(uint4 w, float4 c, float4 s) {
+  return make_uint4(rope_rotate_pair(w.x, c.x, s.x), rope_rotate_pair(w.y, c.y, s.y),
+                    rope_rotate_pair(w.z, c.z, s.z), rope_rotate_pair(w.w, c.w, s.w));
+}
+
 }  // namespace fa

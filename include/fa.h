@@ -112,6 +112,14 @@ FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void
  *   线性偏置") adds -alibi_slopes[h] * |p - j| to every scaled score, p the
  *   query's absolute position (i + Lk - Lq, the causal alignment).  The pages
  *   give no slope values; the caller chooses them.
+ * rope_cos / rope_sin: NULL, or device fp32 tables [rope_rows, rope_dim / 2]: RoPE
+ *   of Q fused into the kernel (jsqmd page, §三 "融合位置编码的Attention计算"): query
+ *   row i is rotated at position p = i + Lk - Lq after it is loaded, pairs of
+ *   adjacent dimensions (2j, 2j+1), j < rope_dim / 2, by (cos, sin)[p, j]; the
+ *   result is rounded to bf16.  K must already be rotated (fa_rope), as it is in a
+ *   KV cache.  rope_dim: multiple of 8, <= d; tables 16-byte aligned.  A query
+ *   position outside [0, rope_rows) leaves that row unrotated and sets bit 1 of
+ *   the device status word.
  */
 typedef struct fa_fwd_args {
   const void* q;
@@ -129,9 +137,24 @@ typedef struct fa_fwd_args {
   int total_q, total_k;
   const int* cu_seqlens_q_host;  /* packed layout, optional host copy for checking */
   const float* alibi_slopes;     /* optional */
+  const float* rope_cos;         /* optional, with rope_sin, rope_rows, rope_dim */
+  const float* rope_sin;
+  int rope_rows, rope_dim;
 } fa_fwd_args;
 
 FA_API fa_status fa_fwd_ex(const fa_fwd_args* args, fa_stream_t stream);
+
+/*
+ * Rotary position embedding in place (the rotary_embedding op of the jsqmd page,
+ * §三): x bf16 [rows, heads, d]; row r is rotated at position positions[r] (device
+ * int32 [rows]) — pairs of adjacent dimensions (2j, 2j+1), j < rotary_dim / 2, by
+ * cos_t / sin_t [table_rows, rotary_dim / 2] (device fp32), fp32 math, bf16
+ * round-to-nearest-even result; dimensions >= rotary_dim are untouched.
+ * rotary_dim: multiple of 8, <= d.  A position outside [0, table_rows) leaves its
+ * row unchanged and sets bit 1 of the device status word.
+ */
+FA_API fa_status fa_rope(void* x, long long rows, int heads, int d, int rotary_dim, const int* positions,
+                         const float* cos_t, const float* sin_t, int table_rows, fa_stream_t stream);
 
 /*
  * Bytes of fp32 workspace fa_decode needs for a given split bound

@@ -185,3 +185,43 @@ def test_alibi_slope_schedule():
     assert s8 == [2.0 ** -(i + 1) for i in range(8)]
     s12 = b.alibi_slopes(12)
     assert s12[:8] == s8 and s12[8:] == [2.0 ** -(0.5 + i) for i in range(4)]
+
+
+def test_rope_arguments_checked(lib):
+    # fa_fwd_args' rope fields sit after alibi_slopes and each is validated on the host
+    _, b = _binding()
+    L = b.load_library()
+    d = 0x1000
+    base = dict(q=d, k=d, v=d, o=d, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=64, scale=0.1)
+    a = b.FwdArgs(**base, rope_cos=d)                                   # sin missing
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"rope_sin" in L.fa_last_error()
+    a = b.FwdArgs(**base, rope_cos=d, rope_sin=d, rope_rows=16, rope_dim=12)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"rope_dim" in L.fa_last_error()
+    a = b.FwdArgs(**base, rope_cos=d, rope_sin=d, rope_rows=16, rope_dim=128)   # > d
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"rope_dim" in L.fa_last_error()
+    a = b.FwdArgs(**base, rope_cos=d, rope_sin=d, rope_rows=0, rope_dim=64)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"rope_rows" in L.fa_last_error()
+    a = b.FwdArgs(**base, rope_cos=d + 4, rope_sin=d, rope_rows=16, rope_dim=64)
+    assert L.fa_fwd_ex(ctypes.byref(a), None) == 1 and b"aligned" in L.fa_last_error()
+    # fa_rope(x, rows, heads, d, rotary_dim, positions, cos, sin, table_rows, stream)
+    L.fa_rope.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert L.fa_rope(None, 4, 2, 64, 64, d, d, d, 8, None) == 1
+    assert L.fa_rope(d, 4, 2, 64, 60, d, d, d, 8, None) == 1 and b"rotary_dim" in L.fa_last_error()
+    assert L.fa_rope(d, 4, 2, 64, 72, d, d, d, 8, None) == 1
+    assert L.fa_rope(d, -1, 2, 64, 64, d, d, d, 8, None) == 1
+    assert L.fa_rope(d, 4, 2, 64, 64, d, d + 8, d, 8, None) == 1 and b"aligned" in L.fa_last_error()
+    assert L.fa_rope(d, 0, 2, 64, 64, d, d, d, 8, None) == 0                  # nothing to do
+
+
+def test_rope_tables_match_oracle_tables():
+    # the binding's table helper builds the same angles as the oracle's (both from
+    # p * base^(-2i / rotary_dim)); fp32 rounding of the fp64 values is the only difference
+    import numpy as np
+    from oracle import rope as orope
+    _, b = _binding()
+    c, s = b.rope_tables(300, 64, device="cpu")
+    rc, rs = orope.tables(300, 64)
+    assert c.dtype.is_floating_point and tuple(c.shape) == (300, 32)
+    np.testing.assert_allclose(c.numpy(), rc, atol=1e-7)
+    np.testing.assert_allclose(s.numpy(), rs, atol=1e-7)

@@ -1,0 +1,136 @@
+"""RoPE (jsqmd page, §三 "RoPE的设计动机与计算特点" and "融合位置编码的Attention计算"):
+the rotation kernel against the oracle's rotation, and the prefill with Q rotated inside
+the kernel (K rotated once beforehand) against the oracle's attention over the oracle's
+rotated Q and K."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import rope as orope
+from fa_workloads import PrefillCase, bf16_bits, make_prefill
+from tests._util import check, gather_prefill_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _tables(max_pos, rd):
+    import flashattention_forward_fa_gb300 as fa
+    return fa.rope_tables(max_pos, rd, device="cuda")
+
+
+@pytest.mark.parametrize("rows,H,d,rd", [(1000, 8, 128, 128), (333, 2, 64, 64), (77, 4, 128, 64), (5, 1, 64, 8)])
+def test_rope_kernel_matches_oracle(rows, H, d, rd):
+    import flashattention_forward_fa_gb300 as fa
+    g = torch.Generator("cpu").manual_seed(rows + rd)
+    x = torch.randn(rows, H, d, generator=g).to(torch.bfloat16)
+    pos = torch.randint(0, 4096, (rows,), generator=g, dtype=torch.int32)
+    cos_t, sin_t = _tables(4096, rd)
+    y = fa.fa_rope(x.cuda(), pos.cuda(), (cos_t, sin_t))
+    torch.cuda.synchronize()
+    # the oracle rotates in fp64 with the same fp32 tables the kernel reads; the kernel works
+    # in fp32, so the two bf16 results agree to one bf16 rounding step
+    ref = orope.rotate_bf16(x, pos.numpy(), cos_t.cpu().double().numpy(), sin_t.cpu().double().numpy(), rd)
+    got = y.cpu()
+    diff = (got.float() - ref.float()).abs()
+    tol = 2.0 ** -7 * ref.float().abs() + 1e-6
+    assert bool((diff <= tol).all()), f"max diff {diff.max().item()}"
+    assert torch.equal(got[..., rd:], x[..., rd:])        # dimensions past rotary_dim untouched
+    assert (got != ref).float().mean().item() < 0.02       # nearly all bit-identical
+    assert fa.fa_device_status() == 0
+
+
+def test_rope_position_out_of_table_reported():
+    import flashattention_forward_fa_gb300 as fa
+    x = torch.randn(4, 2, 64).to(torch.bfloat16).cuda()
+    x0 = x.clone()
+    pos = torch.tensor([0, 1, 99, 2], dtype=torch.int32, device="cuda")
+    fa.fa_device_status(clear=True)
+    fa.fa_rope(x, pos, _tables(16, 64))
+    assert fa.fa_device_status(clear=True) & 2
+    assert torch.equal(x[2], x0[2])
+
+
+def _oracle_rope_prefill(x, case, cos64, sin64, rd):
+    c = case
+    qs, ks = [], []
+    q3 = x.q.reshape(-1, c.Hq, c.d)
+    k3 = x.k.reshape(-1, c.Hkv, c.d)
+    q_pos = np.zeros(q3.shape[0], np.int64)
+    k_pos = np.zeros(k3.shape[0], np.int64)
+    for b in range(len(x.len_q)):
+        lq, lk = x.len_q[b], x.len_k[b]
+        q_pos[x.q_off[b]:x.q_off[b] + lq] = np.arange(lq) + lk - lq    # bottom-right positions
+        k_pos[x.k_off[b]:x.k_off[b] + lk] = np.arange(lk)
+    qr = orope.rotate_bf16(q3, q_pos, cos64, sin64, rd)
+    kr = orope.rotate_bf16(k3, k_pos, cos64, sin64, rd)
+    rows = oracle.all_rows(x.len_q, c.Hq)
+    ro, rl = oracle.attention_rows(bf16_bits(qr), bf16_bits(kr), bf16_bits(x.v.reshape(-1, c.Hkv, c.d)), x.q_off,
+                                   x.len_q, x.k_off, x.len_k, c.softmax_scale, c.causal, c.window, rows)
+    return rows, ro, rl, k_pos
+
+
+@pytest.mark.parametrize("case,rd", [
+    (PrefillCase("rope_causal", B=2, Hq=8, Hkv=8, Nq=700, Nk=700, d=128, causal=True, seed=501), 128),
+    (PrefillCase("rope_gqa_q_lt_k", B=2, Hq=12, Hkv=4, Nq=130, Nk=900, d=128, causal=True, seed=502), 128),
+    (PrefillCase("rope_partial_d64", B=1, Hq=4, Hkv=2, Nq=300, Nk=500, d=64, seed=503), 32),
+    (PrefillCase("rope_window", B=1, Hq=8, Hkv=2, Nq=600, Nk=600, d=128, causal=True, window=200, seed=504), 64),
+    (PrefillCase("rope_varlen", B=3, Hq=4, Hkv=4, Nq=500, Nk=500, d=64, layout="packed", causal=True,
+                 len_q=[500, 17, 256], seed=505), 64),
+], ids=lambda c: c.name if hasattr(c, "name") else str(c))
+def test_fused_rope_prefill_matches_oracle(case, rd):
+    import flashattention_forward_fa_gb300 as fa
+    x = make_prefill(case)
+    cos_t, sin_t = _tables(1024, rd)
+    cos64, sin64 = cos_t.cpu().double().numpy(), sin_t.cpu().double().numpy()
+    rows, ro, rl, k_pos = _oracle_rope_prefill(x, case, cos64, sin64, rd)
+    q, v = x.q.cuda(), x.v.cuda()
+    k = x.k.cuda().clone()
+    fa.fa_rope(k, torch.from_numpy(k_pos).to(torch.int32).cuda(), (cos_t, sin_t))   # K rotated once
+    if case.layout == "packed":
+        cu = torch.tensor([0] + list(np.cumsum(x.len_q)), dtype=torch.int32, device="cuda")
+        o, lse = fa.fa_fwd_varlen(q, k, v, cu, cu, max(x.len_q), max(x.len_k), causal=case.causal,
+                                  window=case.window, scale=case.softmax_scale, rope=(cos_t, sin_t))
+    else:
+        o, lse = fa.fa_fwd(q, k, v, causal=case.causal, window=case.window, scale=case.softmax_scale,
+                           rope=(cos_t, sin_t))
+    torch.cuda.synchronize()
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    check(go, gl, ro, rl, case.name)
+    assert fa.fa_device_status() == 0
+
+
+def test_fused_rope_with_alibi():
+    # both position schemes at once exercise the <ALIBI, ROPE> kernel variant
+    import flashattention_forward_fa_gb300 as fa
+    case = PrefillCase("rope_alibi", B=1, Hq=4, Hkv=4, Nq=400, Nk=400, d=128, causal=True, seed=506)
+    x = make_prefill(case)
+    cos_t, sin_t = _tables(512, 128)
+    cos64, sin64 = cos_t.cpu().double().numpy(), sin_t.cpu().double().numpy()
+    slopes = np.array(fa.alibi_slopes(4), np.float32)
+    q3, k3 = x.q.reshape(-1, 4, 128), x.k.reshape(-1, 4, 128)
+    qr = orope.rotate_bf16(q3, np.arange(400), cos64, sin64, 128)
+    kr = orope.rotate_bf16(k3, np.arange(400), cos64, sin64, 128)
+    rows = oracle.all_rows(x.len_q, 4)
+    ro, rl = oracle.attention_rows(bf16_bits(qr), bf16_bits(kr), bf16_bits(x.v.reshape(-1, 4, 128)), x.q_off,
+                                   x.len_q, x.k_off, x.len_k, case.softmax_scale, True, 0, rows,
+                                   alibi_slopes=slopes.astype(np.float64))
+    k = x.k.cuda().clone()
+    fa.fa_rope(k, torch.arange(400, dtype=torch.int32, device="cuda"), (cos_t, sin_t))
+    o, lse = fa.fa_fwd(x.q.cuda(), k, x.v.cuda(), causal=True, alibi_slopes=slopes, rope=(cos_t, sin_t))
+    torch.cuda.synchronize()
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    check(go, gl, ro, rl, case.name)
+    assert fa.fa_device_status() == 0
+
+
+def test_query_position_past_table_reported():
+    import flashattention_forward_fa_gb300 as fa
+    x = make_prefill(PrefillCase("short_table", B=1, Hq=2, Hkv=2, Nq=200, Nk=200, d=64, seed=507))
+    cos_t, sin_t = _tables(100, 64)       # positions 100..199 have no table row
+    fa.fa_device_status(clear=True)
+    o, lse = fa.fa_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), rope=(cos_t, sin_t))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) & 2
+    assert torch.isfinite(o.float()).all()
