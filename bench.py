@@ -43,7 +43,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from fa_workloads import DECODE_CACHE, LLAMA7B_CAUSAL, make_decode, make_prefill  # noqa: E402
+from fa_workloads import (BERT_VARLEN, DECODE_CACHE, GQA_WINDOW, LLAMA7B_CAUSAL, TINY_MHA,  # noqa: E402
+                          make_decode, make_prefill)
 
 METRIC = "attention fwd TFLOP/s (prefill) & decode GB/s on 1 GB300, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -396,6 +397,9 @@ def gpu_arm(args, world, rank, local):
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_rows:
+        out["rows"] = row_measurements(args, dev, stream, peaks,
+                                       (pc, px, q, k, v, dc, dx, dq, kc, vc, lens, lens_host))
     return out
 
 
@@ -429,6 +433,126 @@ def single_kernel_run(args, dev, stream):
     ok = fa.fa_device_status() == 0
     return {"partial": True, "only": args.only, "value": round(work / (ms * 1e-3), 2), "unit": unit,
             "ms": round(ms, 4), "steps": args.steps, "warmup": args.warmup, "status_ok": ok}
+
+
+# ----------------------------------------------------------------------------- the other workloads and options
+
+def time_alone(fn, steps: int, warmup: int, stream) -> float:
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    (ms,), _ = time_steps([fn], steps, stream)
+    return ms
+
+
+def row_measurements(args, dev, stream, peaks, step_inputs):
+    """The workloads other than the step's own and the option paths (several new tokens over a
+    KV cache, a paged cache, RoPE, ALiBi), each timed alone with CUDA events on the launching
+    stream after its own warm-up.  Prefill rows count algorithmic FLOPs (4 d per visible pair),
+    decode-like rows algorithmic bytes (each valid cached K/V byte once per KV head, q, o, LSE)."""
+    import flashattention_forward_fa_gb300 as fa
+    steps, warm = max(3, min(args.steps, 50)), max(3, args.warmup)
+    tf_peak, gb_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    rows = {}
+
+    def add(name, workload, ms, work, unit, bound, l2):
+        val = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        peak = tf_peak if bound == "tensor" else gb_peak
+        rows[name] = {"workload": workload, "ms": round(ms, 4), "value": round(val, 2), "unit": unit,
+                      "bound": bound, "frac": round(val / peak, 4), "inputs_vs_l2": l2}
+
+    def prefill_row(name, case, desc, l2, **kw):
+        x = make_prefill(case)
+        q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        if case.layout == "packed":
+            cu = torch.tensor([0] + list(np.cumsum(x.len_q)), dtype=torch.int32, device=dev)
+            host = [0] + [int(c) for c in np.cumsum(x.len_q)]
+            fn = lambda: fa.fa_fwd_varlen(q, k, v, cu, cu, max(x.len_q), max(x.len_k), causal=case.causal,  # noqa
+                                          window=case.window, scale=case.softmax_scale, cu_seqlens_q_host=host)
+        else:
+            fn = lambda: fa.fa_fwd(q, k, v, causal=case.causal, window=case.window,  # noqa: E731
+                                   scale=case.softmax_scale, **kw)
+        add(name, desc, time_alone(fn, steps, warm, stream), prefill_flops(case, x.len_q, x.len_k), "TFLOP/s",
+            "tensor", l2)
+
+    prefill_row("tiny_mha", TINY_MHA, "B=1, H=2, N=256, d=64, non-causal (launch-bound)", "inside L2")
+    prefill_row("bert_varlen", BERT_VARLEN, "B=8, H=12, d=64, len U[128,512] packed, non-causal", "inside L2")
+    prefill_row("gqa_window", GQA_WINDOW, "B=4, Hq=32, Hkv=8, N=4096, d=128, causal, window 1024",
+                "larger than L2 (320 MB)")
+
+    pc, px, q, k, v, dc, dx, dq, kc, vc, lens, lens_host = step_inputs
+    o = torch.empty_like(q)
+    # ALiBi on the step's prefill and decode workloads
+    slopes = torch.tensor(fa.alibi_slopes(pc.Hq), dtype=torch.float32, device=dev)
+    flops = prefill_flops(pc, px.len_q, px.len_k)
+    ms = time_alone(lambda: fa.fa_fwd(q, k, v, causal=True, scale=pc.softmax_scale, out=o, alibi_slopes=slopes),
+                    steps, warm, stream)
+    add("alibi_prefill", "llama7b_causal + ALiBi (geometric slopes)", ms, flops, "TFLOP/s", "tensor",
+        "larger than L2")
+    dslopes = torch.tensor(fa.alibi_slopes(dc.Hq), dtype=torch.float32, device=dev)
+    do = torch.empty_like(dq)
+    dbytes = decode_bytes(dc, lens_host)
+    ms = time_alone(lambda: fa.fa_decode(dq, kc, vc, lens, scale=dc.softmax_scale, seqlens_k_host=lens_host,
+                                         out=do, alibi_slopes=dslopes), steps, warm, stream)
+    add("alibi_decode", "decode_cache + ALiBi", ms, dbytes, "GB/s", "hbm", "larger than L2 (2.1 GB)")
+
+    # RoPE: Q rotated inside the prefill kernel (K rotated once beforehand, as in a cache) ...
+    cos_t, sin_t = fa.rope_tables(pc.Nk, pc.d, device=dev)
+    kr = k.clone()
+    fa.fa_rope(kr, torch.arange(pc.Nk, dtype=torch.int32, device=dev).repeat(pc.B), (cos_t, sin_t))
+    ms = time_alone(lambda: fa.fa_fwd(q, kr, v, causal=True, scale=pc.softmax_scale, out=o, rope=(cos_t, sin_t)),
+                    steps, warm, stream)
+    add("rope_prefill", "llama7b_causal, Q rotated in the kernel (rotary_dim 128)", ms, flops, "TFLOP/s", "tensor",
+        "larger than L2")
+    del kr
+    # ... and the in-place rotation pass itself over a 256 MB K block (4 x 8192 rows)
+    xr = torch.randn(4 * pc.Nk, pc.Hkv, pc.d, device=dev).to(torch.bfloat16)
+    pos = torch.arange(pc.Nk, dtype=torch.int32, device=dev).repeat(4)
+    ms = time_alone(lambda: fa.fa_rope(xr, pos, (cos_t, sin_t)), steps, warm, stream)
+    rbytes = 2 * xr.numel() * 2 + pos.numel() * 4
+    add("rope_k", "fa_rope in place, [32768, 32, 128] bf16, rotary_dim 128", ms, rbytes, "GB/s", "hbm",
+        "larger than L2 (256 MB)")
+    del xr
+
+    # several new tokens per sequence over the decode cache (speculative decoding, 4 drafts)
+    nt = 4
+    g = torch.Generator("cpu").manual_seed(6)
+    mq = torch.randn(dc.B, nt, dc.Hq, dc.d, generator=g).to(torch.bfloat16).to(dev)
+    mo = torch.empty_like(mq)
+    ml = torch.empty((dc.B, dc.Hq, nt), dtype=torch.float32, device=dev)
+    S = fa.fa_decode_max_splits(dc.B, dc.Hq, dc.Hkv, dc.Ncap, 0, lens_host, 0)
+    mws = torch.empty((fa.decode_workspace_size(dc.B * nt, dc.Hq, dc.d, S) + 3) // 4, dtype=torch.float32,
+                      device=dev)
+    mbytes = decode_bytes(dc, lens_host) + (nt - 1) * (2 * dc.B * dc.Hq * dc.d * 2 + dc.B * dc.Hq * 4)
+    ms = time_alone(lambda: fa.fa_decode(mq, kc, vc, lens, scale=dc.softmax_scale, seqlens_k_host=lens_host,
+                                         workspace=mws, out=mo, lse=ml), steps, warm, stream)
+    add("multitoken_decode", "decode_cache with 4 new tokens per sequence (bottom-right causal), split-KV decode "
+        "kernel", ms, mbytes, "GB/s", "hbm", "larger than L2 (2.1 GB)")
+    ms = time_alone(lambda: fa.fa_fwd(mq, kc, vc, causal=True, scale=dc.softmax_scale, seqlens_k=lens, out=mo),
+                    steps, warm, stream)
+    add("multitoken_decode_prefill_kernel", "the same through fa_fwd with seqlens_k (128-row Q tiles, 4 used)", ms,
+        mbytes, "GB/s", "hbm", "larger than L2 (2.1 GB)")
+    del mq, mo, mws
+
+    # the decode cache scattered over a page pool (128-token pages in random order)
+    page = 128
+    nb = dc.Ncap // page
+    perm = torch.randperm(dc.B * nb, generator=g).to(dev)
+    kp = torch.empty((dc.B * nb, page, dc.Hkv, dc.d), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    kp[perm] = kc.view(dc.B * nb, page, dc.Hkv, dc.d)
+    vp[perm] = vc.view(dc.B * nb, page, dc.Hkv, dc.d)
+    table = perm.view(dc.B, nb).to(torch.int32).contiguous()
+    ms = time_alone(lambda: fa.fa_decode_paged(dq, kp, vp, table, lens, scale=dc.softmax_scale,
+                                               seqlens_k_host=lens_host, out=do), steps, warm, stream)
+    add("paged_decode", "decode_cache over 128-token pages in random order", ms, dbytes, "GB/s", "hbm",
+        "larger than L2 (2.1 GB)")
+    del kp, vp
+    torch.cuda.synchronize()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("a kernel reported an error while the workload rows ran")
+    rows["note"] = f"each row {steps} launches after {warm} warm-up; frac against the measured peaks"
+    return rows
 
 
 # ----------------------------------------------------------------------------- reference arm (oracle on CPU)
@@ -482,6 +606,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one phase alone (for profilers); prints a partial line")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the per-workload rows (other workloads and option paths) after the step")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0,
                     help="wall time of the oracle CPU baseline sample (rank 0, N=1)")
     args = ap.parse_args()

@@ -37,7 +37,7 @@ class DecodeArgs(ctypes.Structure):
                 ("B", _i), ("Hq", _i), ("Hkv", _i), ("d", _i), ("scale", _f), ("window", _i), ("Ncap", _i),
                 ("block_table", _vp), ("max_blocks", _i), ("page_size", _i), ("num_pages", _i),
                 ("seqlens_k", _vp), ("seqlens_k_host", _ip), ("num_splits", _i),
-                ("workspace", _vp), ("workspace_bytes", _sz), ("alibi_slopes", _vp)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("alibi_slopes", _vp), ("Nq", _i)]
 
 
 _SIGS = {
@@ -293,27 +293,31 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
               workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
               lse: Optional[torch.Tensor] = None, return_lse: bool = True, alibi_slopes=None
               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Decode: q [B, Hq, d], caches [B, Ncap, Hkv, d], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
+    """Decode: q [B, Hq, d], caches [B, Ncap, Hkv, d], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq]).
+    With q [B, Nq, Hq, d] the Nq new tokens are the last Nq cache slots (token t at position
+    len - Nq + t, bottom-right causal) -> (O [B, Nq, Hq, d], LSE [B, Hq, Nq])."""
     lib = load_library()
     _need(q, "q")
     _need(k_cache, "k_cache")
     _need(v_cache, "v_cache")
     _need(seqlens_k, "seqlens_k", torch.int32)
-    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
-        raise FAError(FA_ERR_INVALID, "expected q [B,Hq,d] and caches [B,Ncap,Hkv,d]")
-    B, Hq, d = q.shape
+    if q.dim() not in (3, 4) or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise FAError(FA_ERR_INVALID, "expected q [B,Hq,d] or [B,Nq,Hq,d] and caches [B,Ncap,Hkv,d]")
+    B, Hq, d = q.shape[0], q.shape[-2], q.shape[-1]
+    Nq = q.shape[1] if q.dim() == 4 else 1
     _, Ncap, Hkv, _ = k_cache.shape
     host = _host_ints(seqlens_k_host)
     hostp = ctypes.cast(host, _ip) if host is not None else None
     if workspace is None:
-        S = lib.fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window), hostp, int(num_splits))
-        nbytes = lib.fa_decode_workspace_size(B, Hq, d, max(S, 1))
+        S = lib.fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window) + Nq - 1 if window > 0 else 0, hostp,
+                                     int(num_splits))
+        nbytes = lib.fa_decode_workspace_size(B * Nq, Hq, d, max(S, 1))
         workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=q.device)
     o = out if out is not None else torch.empty_like(q)
     if return_lse and lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq, Nq) if q.dim() == 4 else (B, Hq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
-    if alibi_slopes is None:
+    if alibi_slopes is None and q.dim() == 3:
         _check(lib.fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d, sc,
                              int(window), _ptr(seqlens_k), hostp, int(num_splits), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(q)))
@@ -322,7 +326,7 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     a = DecodeArgs(q=_ptr(q), k=_ptr(k_cache), v=_ptr(v_cache), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv, d=d,
                    scale=sc, window=int(window), Ncap=Ncap, seqlens_k=_ptr(seqlens_k), seqlens_k_host=hostp,
                    num_splits=int(num_splits), workspace=_ptr(workspace),
-                   workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp)
+                   workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp, Nq=Nq)
     _check(lib.fa_decode_ex(ctypes.byref(a), _stream(q)))
     return o, lse
 
@@ -333,36 +337,38 @@ def fa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                     return_lse: bool = True, alibi_slopes=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Decode over a paged cache: q [B, Hq, d], pages [num_pages, page_size, Hkv, d],
-    block_table int32 [B, max_blocks], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq])."""
+    block_table int32 [B, max_blocks], seqlens_k int32 [B] -> (O [B, Hq, d], LSE [B, Hq]).
+    q [B, Nq, Hq, d]: Nq new tokens per sequence, as for fa_decode."""
     lib = load_library()
     _need(q, "q")
     _need(k_pages, "k_pages")
     _need(v_pages, "v_pages")
     _need(block_table, "block_table", torch.int32)
     _need(seqlens_k, "seqlens_k", torch.int32)
-    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.shape != k_pages.shape or block_table.dim() != 2:
-        raise FAError(FA_ERR_INVALID, "expected q [B,Hq,d], pages [P,page,Hkv,d], block_table [B,max_blocks]")
-    B, Hq, d = q.shape
+    if q.dim() not in (3, 4) or k_pages.dim() != 4 or v_pages.shape != k_pages.shape or block_table.dim() != 2:
+        raise FAError(FA_ERR_INVALID, "expected q [B,(Nq,)Hq,d], pages [P,page,Hkv,d], block_table [B,max_blocks]")
+    B, Hq, d = q.shape[0], q.shape[-2], q.shape[-1]
+    Nq = q.shape[1] if q.dim() == 4 else 1
     num_pages, page_size, Hkv, _ = k_pages.shape
     max_blocks = block_table.shape[1]
     host = _host_ints(seqlens_k_host)
     hostp = ctypes.cast(host, _ip) if host is not None else None
     if workspace is None:
-        S = lib.fa_decode_max_splits(B, Hq, Hkv, max_blocks * page_size, int(window) + 63 if window > 0 else 0,
-                                     hostp, int(num_splits))
-        nbytes = lib.fa_decode_workspace_size(B, Hq, d, max(S, 1))
+        S = lib.fa_decode_max_splits(B, Hq, Hkv, max_blocks * page_size,
+                                     int(window) + Nq - 1 + 63 if window > 0 else 0, hostp, int(num_splits))
+        nbytes = lib.fa_decode_workspace_size(B * Nq, Hq, d, max(S, 1))
         workspace = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=q.device)
     o = out if out is not None else torch.empty_like(q)
     if return_lse and lse is None:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, Hq, Nq) if q.dim() == 4 else (B, Hq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
-    if alibi_slopes is not None:
+    if alibi_slopes is not None or q.dim() == 4:
         keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
         a = DecodeArgs(q=_ptr(q), k=_ptr(k_pages), v=_ptr(v_pages), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv,
                        d=d, scale=sc, window=int(window), block_table=_ptr(block_table), max_blocks=max_blocks,
                        page_size=page_size, num_pages=num_pages, seqlens_k=_ptr(seqlens_k), seqlens_k_host=hostp,
                        num_splits=int(num_splits), workspace=_ptr(workspace),
-                       workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp)
+                       workspace_bytes=workspace.numel() * workspace.element_size(), alibi_slopes=sp, Nq=Nq)
         _check(lib.fa_decode_ex(ctypes.byref(a), _stream(q)))
         return o, lse
     _check(lib.fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(o), _ptr(lse), B, Hq, Hkv, num_pages,

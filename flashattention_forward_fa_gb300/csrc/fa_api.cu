@@ -368,6 +368,10 @@ fa_status fa_decode_ex(const fa_decode_args* a, fa_stream_t stream) {
   if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u))
     return fail(FA_ERR_INVALID, "alibi_slopes must be 4-byte aligned");
   if (B > 65535) return fail(FA_ERR_INVALID, "B too large");
+  if (a->Nq < 0) return fail(FA_ERR_INVALID, "Nq must be >= 0");
+  const int nq = a->Nq > 1 ? a->Nq : 1;
+  if ((long long)Hkv * (((long long)nq * (Hq / Hkv) + 15) / 16) > 65535 || (long long)B * nq * Hq >= (1LL << 31))
+    return fail(FA_ERR_INVALID, "Nq (%d) too large for one launch", nq);
   const bool paged = a->block_table != nullptr;
   long long rows;  // rows of the K/V tensors as TMA sees them
   int cap;         // keys a sequence can hold
@@ -388,11 +392,12 @@ fa_status fa_decode_ex(const fa_decode_args* a, fa_stream_t stream) {
   }
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
-  // paged chunks start on a 64-key boundary at or below the window start: plan with window + 63
-  const int plan_window = (paged && window > 0) ? window + 63 : window;
+  // the keys of a sequence's Nq tokens span window + Nq - 1 slots; paged chunks start on a 64-key
+  // boundary at or below the window start: plan with 63 more
+  const int plan_window = window > 0 ? window + (nq - 1) + (paged ? 63 : 0) : window;
   const DecodePlan pl =
       plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, a->seqlens_k_host, a->num_splits, di->sm_count);
-  const size_t need = fa_decode_workspace_size(B, Hq, d, pl.max_splits);
+  const size_t need = fa_decode_workspace_size(B * nq, Hq, d, pl.max_splits);
   if (!a->workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
   if (!aligned16(a->workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
   if (a->workspace_bytes < need)
@@ -409,12 +414,13 @@ fa_status fa_decode_ex(const fa_decode_args* a, fa_stream_t stream) {
   p.lse = a->lse;
   p.seqlens_k = a->seqlens_k;
   p.o_part = static_cast<float*>(a->workspace);
-  p.lse_part = p.o_part + (size_t)B * Hq * pl.max_splits * d;
+  p.lse_part = p.o_part + (size_t)B * nq * Hq * pl.max_splits * d;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.Ncap = cap;
   p.group = Hq / Hkv;
+  p.nq = nq;
   p.chunk = pl.chunk;
   p.max_splits = pl.max_splits;
   p.window = window > 0 ? window : 0;

@@ -1,10 +1,12 @@
-// Single-query incremental decode over a KV cache, split along the key axis,
-// for sm_103a.
+// Incremental decode over a KV cache, split along the key axis, for sm_103a.
 //
 // What it computes: for every sequence b and query head h, the attention of the
-// one new token over the cached keys 0 .. len_b-1 (the incremental mode of the
+// new token over the cached keys 0 .. len_b-1 (the incremental mode of the
 // agent.csdn.net BERT walkthrough, 结尾: the new token attends to all cached K/V
 // and the old K/V are not recomputed, so cost is linear in the cache length).
+// With nq > 1 new tokens per sequence (speculative drafts, a chunk of a prompt)
+// they are the last nq cache slots: token t sits at position len_b - nq + t and
+// sees the keys up to its own position (bottom-right causal alignment).
 // The key range is cut into chunks; each chunk yields a partial (O_s, lse_s)
 // and a combine kernel merges them with the log-sum-exp identity
 //     LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) O_s,
@@ -15,10 +17,10 @@
 // KV head group), so the design is about bytes in flight, not MMA width:
 //   one CTA = one (sequence, KV head, chunk); warp 4 streams 64-key K and V
 //   tiles through a TMA + mbarrier ring; warps 0-3 each take 16 keys of a tile
-//   and run Q K^T and P V on the tensor cores with mma.sync m16n8k16 (the G
-//   query heads of the group are the M rows; G <= 16 rows is below the tcgen05
-//   minimum M of 64), keeping a private running max/sum; the four warps merge
-//   in shared memory at the end of the chunk.
+//   and run Q K^T and P V on the tensor cores with mma.sync m16n8k16 (the
+//   nq x G (token, query head) rows of the group are the M rows, 16 per CTA;
+//   a few rows are below the tcgen05 minimum M of 64), keeping a private running
+//   max/sum; the four warps merge in shared memory at the end of the chunk.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -70,9 +72,10 @@ __device__ __forceinline__ uint32_t sw_off(int key, int d8) {
   return (uint32_t)((d8 >> 3) * DecodeCfg<D>::SLAB + key * 128 + (((d8 & 7) ^ (key & 7)) << 4));
 }
 
-// Key range of sequence b: [lo, len) are the keys its query may see; the chunks cover
-// [base, len) with base = lo for a contiguous cache and lo rounded down to a multiple of 64 for
-// a paged one (so that no 64-key tile straddles two pages; keys below lo are then masked).
+// Key range of sequence b: [lo, len) holds every key one of its nq queries may see (lo is the
+// window start of the first new token); the chunks cover [base, len) with base = lo for a
+// contiguous cache and lo rounded down to a multiple of 64 for a paged one (so that no 64-key
+// tile straddles two pages; keys below a row's own window start are masked).
 struct DecodeRange {
   int len, lo, base;
 };
@@ -80,7 +83,7 @@ __device__ __forceinline__ DecodeRange decode_range(const DecodeParams& p, int b
   DecodeRange r;
   const int cap = paged ? p.max_blocks * p.page_size : p.Ncap;
   r.len = min(max(p.seqlens_k[b], 0), cap);
-  r.lo = p.window > 0 ? max(0, r.len - p.window) : 0;
+  r.lo = p.window > 0 ? max(0, r.len - p.nq + 1 - p.window) : 0;
   r.base = paged ? (r.lo & ~63) : r.lo;
   return r;
 }
@@ -108,19 +111,19 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
   using C = DecodeCfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x;
-  const int n_rb = (p.group + 15) / 16;
+  const int n_rows = p.nq * p.group;                 // (token, head) rows of one KV head
+  const int n_rb = (n_rows + 15) / 16;
   const int hkv = blockIdx.y / n_rb;
   const int rb = blockIdx.y % n_rb;
   const int b = blockIdx.z;
   const DecodeRange kr = decode_range(p, b, PAGED);
-  const int len = kr.len, lo = kr.lo;
+  const int len = kr.len;
   const int start = kr.base + split * p.chunk;
   const int end = min(start + p.chunk, len);
   if (start >= end) return;  // chunk past the end of this sequence's keys
   const int n_tiles = (end - start + C::BN - 1) / C::BN;
-  const int row0 = rb * 16;                          // first query row of this block within the group
-  const int nrows = min(16, p.group - row0);
-  const int hq0 = hkv * p.group + row0;
+  const int row0 = rb * 16;                          // first row of this block: row r is token r / group,
+  const int nrows = min(16, n_rows - row0);          // query head hkv * group + r % group
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,14 +172,23 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 
   // -------------------------------------------------------------- compute warps
   const int g = lane >> 2, tq = lane & 3;
-  // Q fragments (rows = query heads of this block, zero past nrows)
+  const bool v0 = g < nrows, v1 = g + 8 < nrows;  // this lane's two rows exist
+  const int ra = row0 + (v0 ? g : 0), rb8 = row0 + (v1 ? g + 8 : 0);
+  const int ta = ra / p.group, tb = rb8 / p.group;                 // their tokens
+  const int hqa = hkv * p.group + ra % p.group, hqb = hkv * p.group + rb8 % p.group;
+  const size_t qia = ((size_t)b * p.nq + ta) * p.Hq + hqa, qib = ((size_t)b * p.nq + tb) * p.Hq + hqb;
+  // each row's visible keys [klo, khi) cut to this chunk: position pos = len - nq + token
+  const int posa = len - p.nq + ta, posb = len - p.nq + tb;
+  const int kloa = p.window > 0 ? max(0, posa - p.window + 1) : 0;
+  const int klob = p.window > 0 ? max(0, posb - p.window + 1) : 0;
+  const int khia = min(posa + 1, end), khib = min(posb + 1, end);
+  // Q fragments (zero past nrows)
   uint32_t qa[D / 16][4];
   {
-    const uint32_t* qrow_g = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + hq0 + g) * D);
-    const uint32_t* qrow_g8 = reinterpret_cast<const uint32_t*>(
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.Hq + hq0 + g + 8) * D);
-    const bool v0 = g < nrows, v1 = g + 8 < nrows;
+    const uint32_t* qrow_g =
+        reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + qia * D);
+    const uint32_t* qrow_g8 =
+        reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + qib * D);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       qa[kk][0] = v0 ? qrow_g[kk * 8 + tq] : 0u;
@@ -189,11 +201,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  // With ALiBi the scale is applied together with the bias -m_h (pos - key), pos = len - 1 (the new
-  // token is the last cache slot), and everything after works on scaled scores (xs = 1).
+  // With ALiBi the scale is applied together with the bias -m_h (pos - key), pos the row's token
+  // position, and everything after works on scaled scores (xs = 1).
   const float xs = ALIBI ? 1.0f : p.scale_log2;
-  const float slope_g = (ALIBI && g < nrows) ? p.alibi[hq0 + g] * 1.4426950408889634f : 0.f;
-  const float slope_g8 = (ALIBI && g + 8 < nrows) ? p.alibi[hq0 + g + 8] * 1.4426950408889634f : 0.f;
+  const float slope_g = (ALIBI && v0) ? p.alibi[hqa] * 1.4426950408889634f : 0.f;
+  const float slope_g8 = (ALIBI && v1) ? p.alibi[hqb] * 1.4426950408889634f : 0.f;
   float lr0 = 0.f, lr1 = 0.f;  // sums of the bf16-rounded weights P V actually uses (normalise O)
   const uint32_t sbase = smem_u32(sm);
   bool ok = true;
@@ -206,8 +218,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       break;
     }
     const int kb = warp * 16;                              // this warp's keys within the tile
-    const int nvalid = min(16, end - (start + t * C::BN + kb));
-    const int nlow = PAGED ? lo - (start + t * C::BN + kb) : 0;  // keys below the window start
+    const int kw0 = start + t * C::BN + kb;                // its first key
+    const int nvalid = min(16, end - kw0);
     const uint32_t kaddr = sbase + st * C::STAGE;
     const uint32_t vaddr = kaddr + C::TILE;
     if (nvalid > 0) {
@@ -231,21 +243,27 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
         mma_bf16(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
         mma_bf16(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
       }
-      // mask keys past the end
+      // mask keys outside each row's [klo, khi) (this also drops keys past the chunk end)
+      {
+        const int la = kloa - kw0 - 2 * tq, ha = khia - kw0 - 2 * tq;
+        const int lb = klob - kw0 - 2 * tq, hb = khib - kw0 - 2 * tq;
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (n * 8 + 2 * tq + (e & 1) >= nvalid || (PAGED && n * 8 + 2 * tq + (e & 1) < nlow))
-            sc[n][e] = -INFINITY;
+          for (int e = 0; e < 4; ++e) {
+            const int kr = n * 8 + (e & 1);
+            if (e < 2 ? (kr < la || kr >= ha) : (kr < lb || kr >= hb)) sc[n][e] = -INFINITY;
+          }
+      }
       if (ALIBI) {
-        const float dist0 = (float)(len - 1 - (start + t * C::BN + kb + 2 * tq));  // pos - key of e = 0, n = 0
+        const float da = (float)(posa - kw0 - 2 * tq), db = (float)(posb - kw0 - 2 * tq);  // pos - key, n=e=0
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             sc[n][e] = fmaf(sc[n][e], p.scale_log2,
-                            -(e < 2 ? slope_g : slope_g8) * (dist0 - (float)(n * 8 + (e & 1))));
+                            e < 2 ? -slope_g * (da - (float)(n * 8 + (e & 1)))
+                                  : -slope_g8 * (db - (float)(n * 8 + (e & 1))));
       }
       float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -352,32 +370,39 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
         osum += mo[(w * 16 + r) * D + d] * f;
       }
     }
-    const size_t prow = ((size_t)b * p.Hq + hq0 + r) * p.max_splits + split;
+    const int row = row0 + r;
+    const size_t qi = ((size_t)b * p.nq + row / p.group) * p.Hq + hkv * p.group + row % p.group;
+    const size_t prow = qi * p.max_splits + split;
     p.o_part[prow * D + d] = rsum > 0.f ? osum / rsum : 0.f;
     if (d == 0) p.lse_part[prow] = lsum > 0.f ? (mstar + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
-// One warp per (sequence, query head): merge the chunk partials.
+// One warp per (sequence, new token, query head): merge the chunk partials.  O is
+// [B, nq, Hq, d]; LSE is [B, Hq, nq].
 template <int D>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
   const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (warp_global >= p.B * p.Hq) return;
-  const int b = warp_global / p.Hq, hq = warp_global % p.Hq;
+  if (warp_global >= p.B * p.nq * p.Hq) return;
+  const int bt = warp_global / p.Hq, hq = warp_global % p.Hq;
+  const int b = bt / p.nq, t = bt % p.nq;
   const DecodeRange kr = decode_range(p, b, p.page_size > 0);
-  const int nkeys = kr.len - kr.lo;
+  const int pos = kr.len - p.nq + t;  // this token's position; it sees keys (pos - window, pos]
+  const int klo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
+  const int nkeys = pos + 1 - klo;
   const int nspan = kr.len - kr.base;  // keys the chunks cover
   constexpr int PER = D / 32;  // output columns per lane
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)b * p.Hq + hq) * D + lane * PER;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bt * p.Hq + hq) * D + lane * PER;
+  float* lse_out = p.lse ? p.lse + ((size_t)b * p.Hq + hq) * p.nq + t : nullptr;
   if (nkeys <= 0) {
 #pragma unroll
     for (int j = 0; j < PER; ++j) orow[j] = __float2bfloat16(0.f);
-    if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = -INFINITY;
+    if (lse_out && lane == 0) *lse_out = -INFINITY;
     return;
   }
   const int ns = min((nspan + p.chunk - 1) / p.chunk, p.max_splits);  // never read past the workspace
-  const size_t prow0 = ((size_t)b * p.Hq + hq) * p.max_splits;
+  const size_t prow0 = ((size_t)bt * p.Hq + hq) * p.max_splits;
   constexpr float LOG2E = 1.4426950408889634f;
   float mx = -INFINITY;
   for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, p.lse_part[prow0 + s]);
@@ -410,7 +435,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   } else {
     *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
-  if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = mx + __logf(tot);
+  if (lse_out && lane == 0) *lse_out = mx + __logf(tot);
 }
 
 template <int D, bool PAGED, bool ALIBI>
@@ -428,12 +453,12 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  const int n_rb = (p.group + 15) / 16;
+  const int n_rb = (p.nq * p.group + 15) / 16;
   dim3 grid(p.max_splits, p.Hkv * n_rb, p.B);
   fa_decode_split_kernel<D, PAGED, ALIBI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int warps = p.B * p.Hq;
+  const int warps = p.B * p.nq * p.Hq;
   fa_decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -39,13 +39,14 @@ struct RopeParams {
 cudaError_t launch_rope(const RopeParams& p, int sm_count, cudaStream_t stream);
 
 struct DecodeParams {
-  const void* q;           // bf16 [B, Hq, d]
-  void* o;                 // bf16 [B, Hq, d]
-  float* lse;              // fp32 [B, Hq] or nullptr
+  const void* q;           // bf16 [B, nq, Hq, d]
+  void* o;                 // bf16 [B, nq, Hq, d]
+  float* lse;              // fp32 [B, Hq, nq] or nullptr
   const int* seqlens_k;    // int32 [B]
-  float* o_part;           // fp32 [B, Hq, max_splits, d]
-  float* lse_part;         // fp32 [B, Hq, max_splits]
+  float* o_part;           // fp32 [B, nq, Hq, max_splits, d]
+  float* lse_part;         // fp32 [B, nq, Hq, max_splits]
   int B, Hq, Hkv, Ncap, group;
+  int nq;                  // new tokens per sequence (the last nq cache slots)
   int chunk;               // keys per split (multiple of 64)
   int max_splits;
   int window;

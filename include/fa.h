@@ -212,6 +212,19 @@ FA_API fa_status fa_decode_paged(const void* q, const void* k_pages, const void*
  * are the page pools, num_pages/page_size/max_blocks describe them), else
  * contiguous [B, Ncap, Hkv, d] (as fa_decode).  alibi_slopes as in fa_fwd_args:
  * the new token sits at position len - 1, so key j gets -m_h * (len - 1 - j).
+ *
+ * Nq (0 or 1: one token): new tokens per sequence, for speculative decoding or a
+ * chunk of a prompt on top of a cache (the incremental mode of the agent.csdn.net
+ * BERT walkthrough, 结尾, with several new tokens).  They are the last Nq cache
+ * slots: token t of sequence b sits at position p = len_b - Nq + t and sees keys
+ * j <= p (and j > p - window), the bottom-right alignment of fa_fwd.  Layouts:
+ * q, o [B, Nq, Hq, d]; lse [B, Hq, Nq].  Tokens with p < 0 see no keys (O = 0,
+ * LSE = -inf).  One CTA takes 16 (token, head) rows of a KV head, so K/V are read
+ * ceil(Nq * Hq/Hkv / 16) times per KV head (from L2 when they are resident); for
+ * long chunks fa_fwd with seqlens_k is the better path.
+ * Workspace: fa_decode_workspace_size(B * Nq, Hq, d, S) with S from
+ * fa_decode_max_splits(B, Hq, Hkv, cap, window > 0 ? window + Nq - 1 : 0, ...)
+ * (paged: window + Nq - 1 + 63), cap = Ncap or max_blocks * page_size.
  */
 typedef struct fa_decode_args {
   const void* q;
@@ -231,6 +244,7 @@ typedef struct fa_decode_args {
   void* workspace;
   size_t workspace_bytes;
   const float* alibi_slopes;     /* optional */
+  int Nq;                        /* new tokens per sequence; 0 or 1 = one */
 } fa_decode_args;
 
 FA_API fa_status fa_decode_ex(const fa_decode_args* args, fa_stream_t stream);
