@@ -241,7 +241,7 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
     p.rope_rows = a->rope_rows;
     p.rope_dim = a->rope_dim;
   }
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_rows, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_rows, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }

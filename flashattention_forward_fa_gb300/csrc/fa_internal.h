@@ -24,6 +24,7 @@ struct PrefillParams {
   const float* rope_cos;
   const float* rope_sin;
   int rope_rows, rope_dim;
+  int n_qblk;              // 256-row blocks per sequence (set by the launcher)
 };
 
 struct RopeParams {
@@ -61,7 +62,7 @@ struct DecodeParams {
 
 // max_rows: rows per sequence (padded layout) or the longest sequence (packed layout).
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int max_rows, cudaStream_t stream);
+                           const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream);
 int prefill_box_rows();  // rows of one TMA box of Q / K / V
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,

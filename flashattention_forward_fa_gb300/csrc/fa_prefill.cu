@@ -9,7 +9,12 @@
 // realised as a running max whose changes rescale the accumulator).
 //
 // How (GB300-first; the pages' Cube/Vector double buffer is only prior art):
-//   one CTA = two 128-row Q tiles (A, B) of one (sequence, query head); 12 warps:
+//   persistent: one CTA per SM walks its share of the work items (a snake over the
+//   CTAs of the heaviest-first item list); one item = two 128-row Q tiles (A, B) of
+//   one (sequence, query head).  The K/V rings and every barrier phase run on across
+//   items, so the next item's Q load, K/V loads and first S overlap the current
+//   item's last P V and epilogue instead of a CTA launch, TMEM allocation and
+//   pipeline fill per item.  12 warps:
 //     warps 0-3   softmax of tile A: thread r owns score row r (TMEM lane r)
 //     warps 4-7   softmax of tile B
 //     warp  8     TMA producer for Q (once) and the K ring
@@ -60,8 +65,8 @@ struct PrefillCfg {
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
   // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2;
+  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2], q_empty
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
@@ -177,32 +182,54 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// One work item: two consecutive 128-row Q tiles of one (sequence, query head).
+struct WorkItem {
+  int h, q0;
+  SeqInfo s;
+  QTileRange ra, rb;
+  int u0, u1;  // union of the two tiles' K/V tile ranges (contiguous: tile B's rows follow
+               // tile A's, so B's first visible key is at most one past A's last); empty if u0 >= u1
+  bool live;   // the block holds output rows (q0 < rows_out)
+};
+
+// Item w: query head fastest, then sequence, then 256-row block; masked problems (causal or
+// window) take the blocks latest-first, which is heaviest-first for causal.
+template <int BM, int BN>
+__device__ __forceinline__ WorkItem work_item(const PrefillParams& p, int w) {
+  WorkItem it;
+  it.h = w % p.Hq;
+  const int rest = w / p.Hq;
+  const int b = rest % p.B;
+  const int j = rest / p.B;
+  const int qblk = (p.causal || p.window > 0) ? p.n_qblk - 1 - j : j;
+  it.q0 = qblk * (2 * BM);
+  it.s = seq_info(p, b, it.h);
+  it.live = it.q0 < it.s.rows_out;
+  it.ra = qtile_range<BM, BN>(it.s, it.q0, p.causal, p.window);
+  it.rb = qtile_range<BM, BN>(it.s, it.q0 + BM, p.causal, p.window);
+  const bool act_a = it.ra.t1 > it.ra.t0, act_b = it.rb.t1 > it.rb.t0;
+  it.u0 = act_a ? (act_b ? min(it.ra.t0, it.rb.t0) : it.ra.t0) : (act_b ? it.rb.t0 : 0);
+  it.u1 = act_a ? (act_b ? max(it.ra.t1, it.rb.t1) : it.ra.t1) : (act_b ? it.rb.t1 : 0);
+  return it;
+}
+
+// The k-th item of this CTA: a snake over the resident CTAs (round k runs forward for even k,
+// backward for odd k), which evens out the decreasing costs of heaviest-first items.  -1 when
+// round k has no item for this CTA.
+__device__ __forceinline__ int snake_item(int k, int n_items) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long w = (k & 1) ? (k + 1) * G - 1 - c : k * G + c;
+  return w < n_items ? (int)w : -1;
+}
+
 template <int D, bool ALIBI, bool ROPE>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using C = PrefillCfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x;
-  const int b = blockIdx.z;
-  const int qblk = (p.causal || p.window > 0) ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
-  const int q0 = qblk * (C::NQT * C::BM);
-  const SeqInfo s = seq_info(p, b, h);
-  if (q0 >= s.rows_out) return;  // whole block past the (padded) end
-  const int hkv = h / p.group;
-
-  const QTileRange ra = qtile_range<C::BM, C::BN>(s, q0, p.causal, p.window);
-  const QTileRange rb = qtile_range<C::BM, C::BN>(s, q0 + C::BM, p.causal, p.window);
-  const bool act_a = ra.t1 > ra.t0, act_b = rb.t1 > rb.t0;
-  if (!act_a && !act_b) {  // no row of the block sees a key: O = 0, LSE = -inf (and zero padding rows)
-    for (int r = tid; r < C::NQT * C::BM; r += blockDim.x)
-      if (q0 + r < s.rows_out) store_row_zero<D>(p, s, h, q0 + r);
-    return;
-  }
-  // Union of the two tiles' K/V ranges.  It is contiguous: tile B's rows directly follow
-  // tile A's, so B's first visible key is at most one past A's last.
-  const int u0 = act_a ? (act_b ? min(ra.t0, rb.t0) : ra.t0) : rb.t0;
-  const int u1 = act_a ? (act_b ? max(ra.t1, rb.t1) : ra.t1) : rb.t1;
+  const int n_items = p.Hq * p.B * p.n_qblk;
+  const int n_rounds = (int)(((long long)n_items + gridDim.x - 1) / gridDim.x);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,16 +237,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint64_t* bar_q = bars;
+  uint64_t* bar_q = bars;               // Q of an item landed
   uint64_t* k_full = bar_q + 1;
   uint64_t* k_empty = k_full + C::KST;
   uint64_t* v_full = k_empty + C::KST;
   uint64_t* v_empty = v_full + C::VST;
   uint64_t* s_full = v_empty + C::VST;  // [2]: one completion per S of tile X
   uint64_t* p_full = s_full + 2;        // [2]: four warp arrivals per P of tile X
-  uint64_t* o_final = p_full + 2;       // [2]: single completion, the last PV of tile X
+  uint64_t* o_final = p_full + 2;       // [2]: one completion per item, the last PV of tile X
   uint64_t* mma_done = o_final + 2;
   uint64_t* q_ready = mma_done + 1;     // [2]: four warp arrivals once Q_X is rotated (RoPE only)
+  uint64_t* q_empty = q_ready + 2;      // every S of an item has run: Q may be overwritten
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
 
@@ -242,6 +270,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     mbar_init(mma_done, 1);
     mbar_init(&q_ready[0], 4);
     mbar_init(&q_ready[1], 4);
+    mbar_init(q_empty, 1);
     fence_barrier_init();
   }
   if (warp == 10) {
@@ -253,164 +282,181 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Every role walks the same item sequence and derives the same per-item facts, so the
+  // barrier phases below are running counts that continue from one item to the next.
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
     setmaxnreg_inc<C::REGS_SOFTMAX>();
     const int X = warp >> 2;               // 0: tile A, 1: tile B
-    const QTileRange r = X ? rb : ra;
     const int rg = tid & 127;              // row within the tile = TMEM lane
-    const int i = r.q0 + rg;
-    const int pos = i + s.Lk - s.Lq;
-    int row_lo, row_hi;  // this row's visible keys [row_lo, row_hi)
-    visible_keys(pos, s.Lk, p.causal, p.window, row_lo, row_hi);
     const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t colS = C::COL_S + 128u * X, colO = C::COL_O + (uint32_t)D * X;
     // scores are scaled into log2 units by sl2; with ALiBi the scale is applied together with
     // the bias below and everything after works on already-scaled scores (xs = 1)
     const float sl2 = p.scale_log2;
     const float xs = ALIBI ? 1.0f : sl2;
-    const float slope2 = ALIBI ? p.alibi[h] * 1.4426950408889634f : 0.f;  // m_h in log2 units
-    float m = -INFINITY;  // running max used for exponentiation (log2 units)
-    float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
-    float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
+    uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full / p_full phase)
+    uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
+    uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
     bool ok = true;
-    if (ROPE) {
-      // Rotate this thread's Q row (position pos) in place: 16-byte chunks of the 128-byte swizzled
-      // rows the TMA wrote, four adjacent pairs per chunk.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort_flag, p.err));
-      if (ok && i < s.Lq) {
-        if (pos >= 0 && pos < p.rope_rows) {
-          uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
-          const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
-          const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
-          for (int c = 0; c < p.rope_dim / 8; ++c) {
-            uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
-            *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
-                               *reinterpret_cast<const float4*>(st + 4 * c));
+    for (int k = 0; ok && k < n_rounds; ++k) {
+      const int w = snake_item(k, n_items);
+      if (w < 0) continue;
+      const WorkItem it = work_item<C::BM, C::BN>(p, w);
+      if (!it.live) continue;
+      const SeqInfo s = it.s;
+      const QTileRange r = X ? it.rb : it.ra;
+      const int h = it.h;
+      const int i = r.q0 + rg;
+      if (it.u1 > it.u0) ++n_q;
+      if (r.t1 <= r.t0) {  // this tile's rows see no key: O = 0, LSE = -inf (and zero padding rows)
+        if (i < s.rows_out) store_row_zero<D>(p, s, h, i);
+        continue;
+      }
+      const int pos = i + s.Lk - s.Lq;
+      int row_lo, row_hi;  // this row's visible keys [row_lo, row_hi)
+      visible_keys(pos, s.Lk, p.causal, p.window, row_lo, row_hi);
+      const float slope2 = ALIBI ? p.alibi[h] * 1.4426950408889634f : 0.f;  // m_h in log2 units
+      float m = -INFINITY;  // running max used for exponentiation (log2 units)
+      float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
+      float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
+      if (ROPE) {
+        // Rotate this thread's Q row (position pos) in place: 16-byte chunks of the 128-byte
+        // swizzled rows the TMA wrote, four adjacent pairs per chunk.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
+        if (ok && i < s.Lq) {
+          if (pos >= 0 && pos < p.rope_rows) {
+            uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
+            const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
+            const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
+            for (int c = 0; c < p.rope_dim / 8; ++c) {
+              uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
+              *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
+                                 *reinterpret_cast<const float4*>(st + 4 * c));
+            }
+          } else {
+            atomicOr(p.err, kDevErrBounds);  // no table row for this position
           }
-        } else {
-          atomicOr(p.err, kDevErrBounds);  // no table row for this position
         }
+        fence_async_smem();  // the MMA reads Q through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_ready[X]);
       }
-      fence_async_smem();  // the MMA reads Q through the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_ready[X]);
-    }
-    for (int t = r.t0; ok && t < r.t1; ++t) {
-      const int n = t - r.t0;
-      ok = mbar_wait(&s_full[X], n & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sc[C::BN];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(t_lane + colS + 0, r0);
-        tmem_ld32(t_lane + colS + 32, r1);
-        tmem_ld32(t_lane + colS + 64, r2);
-        tmem_ld32(t_lane + colS + 96, r3);
-        tmem_ld_wait(r0);
-        tmem_ld_wait(r1);
-        tmem_ld_wait(r2);
-        tmem_ld_wait(r3);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          sc[j] = __uint_as_float(r0[j]);
-          sc[32 + j] = __uint_as_float(r1[j]);
-          sc[64 + j] = __uint_as_float(r2[j]);
-          sc[96 + j] = __uint_as_float(r3[j]);
+      for (int t = r.t0; ok && t < r.t1; ++t, ++n_sx) {
+        const int n = t - r.t0;
+        ok = mbar_wait(&s_full[X], n_sx & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-      }
-      const int k0 = t * C::BN;
-      if (tile_needs_mask<C::BN>(r, k0, s.Lk, p.causal, p.window)) {
-        // keep column j iff k0 + j lies in the row's visible interval: one unsigned compare per key
-        const uint32_t lo = (uint32_t)(row_lo - k0);
-        const uint32_t span = (uint32_t)max(row_hi - row_lo, 0);
+        tc_fence_after();
+        float sc[C::BN];
+        {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(t_lane + colS + 0, r0);
+          tmem_ld32(t_lane + colS + 32, r1);
+          tmem_ld32(t_lane + colS + 64, r2);
+          tmem_ld32(t_lane + colS + 96, r3);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
+          tmem_ld_wait(r2);
+          tmem_ld_wait(r3);
 #pragma unroll
-        for (int j = 0; j < C::BN; ++j)
-          if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
-      }
-      if (ALIBI) {
-        const float dpos = (float)(pos - k0);
-#pragma unroll
-        for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
-      }
-      float mx;
-      {  // row max: eight independent chains of three-input max
-        float t8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
-#pragma unroll
-        for (int j = 24; j < C::BN - 8; j += 16)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) t8[u] = fmax3(t8[u], sc[j + u], sc[j + 8 + u]);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
-        mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
-      }
-      mx *= xs;
-      const float m_new = fmaxf(m, mx);
-      const bool need = m_new > m + 8.0f;  // -inf + 8 = -inf: the first finite max always moves m
-      const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
-      const bool o_live = need && (n > 0) && (m != -INFINITY);  // O row holds data to rescale
-      if (__any_sync(0xffffffffu, o_live)) {
-        // S_X(t) was issued after PV_X(t-1), so O_X is current: rescale it in place.
-        const float f = o_live ? alpha : 1.0f;
-#pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          uint32_t ov[16];
-          tmem_ld16(t_lane + colO + c, ov);
-          tmem_ld_wait(ov);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-          tmem_st16(t_lane + colO + c, ov);
+          for (int j = 0; j < 32; ++j) {
+            sc[j] = __uint_as_float(r0[j]);
+            sc[32 + j] = __uint_as_float(r1[j]);
+            sc[64 + j] = __uint_as_float(r2[j]);
+            sc[96 + j] = __uint_as_float(r3[j]);
+          }
         }
-      }
-      if (need) {
-        l *= alpha;
-        lr *= alpha;
-        m = m_new;
-      }
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      // P V runs on bf16-rounded weights; normalising O by the sum of those same rounded
-      // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
-      // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
-      // (two accumulators each to keep the dependency chains short).
-      const uint64_t sl2x2 = f2_pack(xs, xs), negm2 = f2_pack(-m_use, -m_use);
-      uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-      float lr4[4] = {0.f, 0.f, 0.f, 0.f};
+        const int k0 = t * C::BN;
+        if (tile_needs_mask<C::BN>(r, k0, s.Lk, p.causal, p.window)) {
+          // keep column j iff k0 + j lies in the row's visible interval: one unsigned compare per key
+          const uint32_t lo = (uint32_t)(row_lo - k0);
+          const uint32_t span = (uint32_t)max(row_hi - row_lo, 0);
 #pragma unroll
-      for (int c = 0; c < C::BN / 32; ++c) {  // 32 scores -> 16 packed columns, stored at once
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(sc[32 * c + 2 * j], sc[32 * c + 2 * j + 1]), sl2x2, negm2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
-          pk[j] = pack_bf16x2(e0, e1);
-          bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
+          for (int j = 0; j < C::BN; ++j)
+            if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
         }
-        tmem_st16(t_lane + colS + 16 * c, pk);
+        if (ALIBI) {
+          const float dpos = (float)(pos - k0);
+#pragma unroll
+          for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
+        }
+        float mx;
+        {  // row max: eight independent chains of three-input max
+          float t8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
+#pragma unroll
+          for (int j = 24; j < C::BN - 8; j += 16)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t8[u] = fmax3(t8[u], sc[j + u], sc[j + 8 + u]);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
+          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+        }
+        mx *= xs;
+        const float m_new = fmaxf(m, mx);
+        const bool need = m_new > m + 8.0f;  // -inf + 8 = -inf: the first finite max always moves m
+        const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+        const bool o_live = need && (n > 0) && (m != -INFINITY);  // O row holds data to rescale
+        if (__any_sync(0xffffffffu, o_live)) {
+          // S_X(t) was issued after PV_X(t-1), so O_X is current: rescale it in place.
+          const float f = o_live ? alpha : 1.0f;
+#pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            uint32_t ov[16];
+            tmem_ld16(t_lane + colO + c, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+            tmem_st16(t_lane + colO + c, ov);
+          }
+        }
+        if (need) {
+          l *= alpha;
+          lr *= alpha;
+          m = m_new;
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        // P V runs on bf16-rounded weights; normalising O by the sum of those same rounded
+        // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
+        // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
+        // (two accumulators each to keep the dependency chains short).
+        const uint64_t sl2x2 = f2_pack(xs, xs), negm2 = f2_pack(-m_use, -m_use);
+        uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        float lr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < C::BN / 32; ++c) {  // 32 scores -> 16 packed columns, stored at once
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sc[32 * c + 2 * j], sc[32 * c + 2 * j + 1]), sl2x2, negm2), x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
+            pk[j] = pack_bf16x2(e0, e1);
+            bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
+          }
+          tmem_st16(t_lane + colS + 16 * c, pk);
+        }
+        {
+          float a0, a1;
+          f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
+          l += a0 + a1;
+          lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[X]);
       }
-      {
-        float a0, a1;
-        f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
-        l += a0 + a1;
-        lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[X]);
-    }
-    if (r.t1 > r.t0) {
       if (ok) {
-        ok = mbar_wait(&o_final[X], 0, abort_flag, p.err);  // the last PV of this tile finished
+        ok = mbar_wait(&o_final[X], n_ox & 1, abort_flag, p.err);  // the last PV of this tile finished
         ok = __all_sync(0xffffffffu, ok);
       }
+      ++n_ox;
       if (ok) {
         tc_fence_after();
         const bool store = i < s.Lq;
@@ -434,8 +480,6 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         if (store && p.lse) p.lse[s.lse_row0 + i] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         if (!store && i < s.rows_out) store_row_zero<D>(p, s, h, i);
       }
-    } else if (i < s.rows_out) {
-      store_row_zero<D>(p, s, h, i);  // this tile's rows see no key
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ Q + K producer
@@ -443,26 +487,45 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(bar_q, C::NQT * C::Q_BYTES);
+      uint32_t gk = 0;   // K tiles issued (ring index)
+      uint32_t n_q = 0;  // items whose Q was loaded
+      bool ok = true;
+      for (int k = 0; ok && k < n_rounds; ++k) {
+        const int w = snake_item(k, n_items);
+        if (w < 0) continue;
+        const WorkItem it = work_item<C::BM, C::BN>(p, w);
+        if (!it.live || it.u1 <= it.u0) continue;
+        // Q of the previous item is in use until its last S has run
+        if (n_q > 0 && !mbar_wait(q_empty, (n_q - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_q, C::NQT * C::Q_BYTES);
 #pragma unroll
-      for (int X = 0; X < C::NQT; ++X)
+        for (int X = 0; X < C::NQT; ++X)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, bar_q, c * 64, h, s.q_row0 + q0 + X * C::BM);
-      int i = 0;
-      for (; i < u1 - u0; ++i) {
-        const int st = i % C::KST;
-        if (i >= C::KST && !mbar_wait(&k_empty[st], ((i / C::KST) + 1) & 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-        uint8_t* dst = sK + st * C::KV_BYTES;
-        const int row = s.k_row0 + (u0 + i) * C::BN;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, bar_q, c * 64, it.h,
+                        it.s.q_row0 + it.q0 + X * C::BM);
+        ++n_q;
+        const int hkv = it.h / p.group;
+        for (int t = it.u0; t < it.u1; ++t, ++gk) {
+          const uint32_t st = gk % C::KST;
+          if (gk >= (uint32_t)C::KST && !mbar_wait(&k_empty[st], ((gk / C::KST) + 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
+          uint8_t* dst = sK + st * C::KV_BYTES;
+          const int row = it.s.k_row0 + t * C::BN;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_k, &k_full[st], c * 64, hkv, row);
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_k, &k_full[st], c * 64, hkv, row);
+        }
       }
       // drain: every issued load has landed before the CTA may exit
-      mbar_wait(bar_q, 0, abort_flag, nullptr);
-      for (int st = 0; st < C::KST && st < i; ++st) {
-        const int last = st + ((i - 1 - st) / C::KST) * C::KST;
+      if (n_q > 0) mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, nullptr);
+      for (uint32_t st = 0; st < (uint32_t)C::KST && st < gk; ++st) {
+        const uint32_t last = st + ((gk - 1 - st) / C::KST) * C::KST;
         mbar_wait(&k_full[st], (last / C::KST) & 1, abort_flag, nullptr);
       }
     }
@@ -471,18 +534,29 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     setmaxnreg_dec<C::REGS_PRODUCER>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
-      int i = 0;
-      for (; i < u1 - u0; ++i) {
-        const int st = i % C::VST;
-        if (i >= C::VST && !mbar_wait(&v_empty[st], ((i / C::VST) + 1) & 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-        uint8_t* dst = sV + st * C::KV_BYTES;
-        const int row = s.k_row0 + (u0 + i) * C::BN;
+      uint32_t gv = 0;  // V tiles issued (ring index)
+      bool ok = true;
+      for (int k = 0; ok && k < n_rounds; ++k) {
+        const int w = snake_item(k, n_items);
+        if (w < 0) continue;
+        const WorkItem it = work_item<C::BM, C::BN>(p, w);
+        if (!it.live || it.u1 <= it.u0) continue;
+        const int hkv = it.h / p.group;
+        for (int t = it.u0; t < it.u1; ++t, ++gv) {
+          const uint32_t st = gv % C::VST;
+          if (gv >= (uint32_t)C::VST && !mbar_wait(&v_empty[st], ((gv / C::VST) + 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
+          uint8_t* dst = sV + st * C::KV_BYTES;
+          const int row = it.s.k_row0 + t * C::BN;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_v, &v_full[st], c * 64, hkv, row);
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_v, &v_full[st], c * 64, hkv, row);
+        }
       }
-      for (int st = 0; st < C::VST && st < i; ++st) {
-        const int last = st + ((i - 1 - st) / C::VST) * C::VST;
+      for (uint32_t st = 0; st < (uint32_t)C::VST && st < gv; ++st) {
+        const uint32_t last = st + ((gv - 1 - st) / C::VST) * C::VST;
         mbar_wait(&v_full[st], (last / C::VST) & 1, abort_flag, nullptr);
       }
     }
@@ -496,9 +570,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(sV), C::CHUNK, 1024);
-    // S_X = Q_X K_i^T  (i = union index of the K tile)
-    auto issue_s = [&](int X, int i) {
-      const uint64_t kd = k_desc + (uint64_t)(((i % C::KST) * C::KV_BYTES) >> 4);
+    // S_X = Q_X K^T with K from ring slot g % KST
+    auto issue_s = [&](int X, uint32_t g) {
+      const uint64_t kd = k_desc + (uint64_t)(((g % C::KST) * C::KV_BYTES) >> 4);
       const uint64_t qd = q_desc + (uint64_t)((X * C::Q_BYTES) >> 4);
       const uint32_t d_cols = tmem + C::COL_S + 128u * X;
 #pragma unroll
@@ -508,9 +582,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
       umma_commit_by(leader, &s_full[X]);
     };
-    // O_X (+)= P_X V_i, P_X read from TMEM where the softmax left it
-    auto issue_pv = [&](int X, int t, int i, const QTileRange& r) {
-      const uint64_t vd = v_desc + (uint64_t)(((i % C::VST) * C::KV_BYTES) >> 4);
+    // O_X (+)= P_X V with V from ring slot g % VST, P_X read from TMEM where the softmax left it.
+    // The first P V of an item overwrites O_X: the softmax warps read the previous item's O_X
+    // before they arrived on p_full for this item's first tile, which this issue waited for.
+    auto issue_pv = [&](int X, int t, uint32_t g, const QTileRange& r) {
+      const uint64_t vd = v_desc + (uint64_t)(((g % C::VST) * C::KV_BYTES) >> 4);
       const uint32_t p_cols = tmem + C::COL_S + 128u * X;
       const uint32_t d_cols = tmem + C::COL_O + (uint32_t)D * X;
       const uint32_t acc0 = t > r.t0 ? 1u : 0u;
@@ -520,47 +596,70 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
                    kk > 0 ? 1u : acc0);
       if (t == r.t1 - 1) umma_commit_by(leader, &o_final[X]);
     };
-    bool ok = mbar_wait(bar_q, 0, abort_flag, p.err) && mbar_wait(&k_full[0], 0, abort_flag, p.err);
-    if (ROPE)  // the softmax warps rotate Q in place first
-      ok = ok && mbar_wait(&q_ready[0], 0, abort_flag, p.err) && mbar_wait(&q_ready[1], 0, abort_flag, p.err);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      if (act_a && ra.t0 == u0) issue_s(0, 0);
-      if (act_b && rb.t0 == u0) issue_s(1, 0);
-      umma_commit_by(leader, &k_empty[0]);
-    }
-    for (int t = u0; ok && t < u1; ++t) {
-      const int i = t - u0;
-      const bool nxt = t + 1 < u1;
-      bool v_ready = false, k_ready = false;
-#pragma unroll
-      for (int X = 0; X < C::NQT; ++X) {
-        const QTileRange& r = X ? rb : ra;
-        if (t >= r.t0 && t < r.t1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], (t - r.t0) & 1, abort_flag, p.err));
-          if (ok && !v_ready) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[i % C::VST], (i / C::VST) & 1, abort_flag, p.err));
-            v_ready = true;
-          }
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(X, t, i, r);
-        }
-        if (nxt && t + 1 >= r.t0 && t + 1 < r.t1) {
-          if (!k_ready) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&k_full[(i + 1) % C::KST], ((i + 1) / C::KST) & 1, abort_flag, p.err));
-            if (!ok) break;
-            k_ready = true;
-            tc_fence_after();
-          }
-          issue_s(X, i + 1);
-        }
+    uint32_t gk = 0, gv = 0;              // K / V tiles consumed (ring indices)
+    uint32_t n_q = 0;                     // items (bar_q phase)
+    uint32_t n_p[2] = {0, 0};             // P tiles of tile X (p_full phase)
+    uint32_t n_r[2] = {0, 0};             // items with tile X active (q_ready phase)
+    bool ok = true;
+    for (int k = 0; ok && k < n_rounds; ++k) {
+      const int w = snake_item(k, n_items);
+      if (w < 0) continue;
+      const WorkItem it = work_item<C::BM, C::BN>(p, w);
+      if (!it.live || it.u1 <= it.u0) continue;
+      const bool act_a = it.ra.t1 > it.ra.t0, act_b = it.rb.t1 > it.rb.t0;
+      ok = mbar_wait(bar_q, n_q & 1, abort_flag, p.err) &&
+           mbar_wait(&k_full[gk % C::KST], (gk / C::KST) & 1, abort_flag, p.err);
+      ++n_q;
+      if (ROPE) {  // the softmax warps rotate Q in place first
+        if (act_a) ok = ok && mbar_wait(&q_ready[0], n_r[0] & 1, abort_flag, p.err);
+        if (act_b) ok = ok && mbar_wait(&q_ready[1], n_r[1] & 1, abort_flag, p.err);
+        n_r[0] += act_a;
+        n_r[1] += act_b;
       }
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      umma_commit_by(leader, &v_empty[i % C::VST]);
-      if (nxt) umma_commit_by(leader, &k_empty[(i + 1) % C::KST]);
+      tc_fence_after();
+      if (act_a && it.ra.t0 == it.u0) issue_s(0, gk);
+      if (act_b && it.rb.t0 == it.u0) issue_s(1, gk);
+      umma_commit_by(leader, &k_empty[gk % C::KST]);
+      if (it.u1 - it.u0 == 1) umma_commit_by(leader, q_empty);  // every S of the item is issued
+      for (int t = it.u0; ok && t < it.u1; ++t) {
+        const uint32_t gki = gk + (uint32_t)(t - it.u0), gvi = gv + (uint32_t)(t - it.u0);
+        const bool nxt = t + 1 < it.u1;
+        bool v_ready = false, k_ready = false;
+#pragma unroll
+        for (int X = 0; X < C::NQT; ++X) {
+          const QTileRange& r = X ? it.rb : it.ra;
+          if (t >= r.t0 && t < r.t1) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], n_p[X] & 1, abort_flag, p.err));
+            ++n_p[X];
+            if (ok && !v_ready) {
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(&v_full[gvi % C::VST], (gvi / C::VST) & 1, abort_flag, p.err));
+              v_ready = true;
+            }
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(X, t, gvi, r);
+          }
+          if (nxt && t + 1 >= r.t0 && t + 1 < r.t1) {
+            if (!k_ready) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&k_full[(gki + 1) % C::KST], ((gki + 1) / C::KST) & 1,
+                                                     abort_flag, p.err));
+              if (!ok) break;
+              k_ready = true;
+              tc_fence_after();
+            }
+            issue_s(X, gki + 1);
+          }
+        }
+        if (!ok) break;
+        umma_commit_by(leader, &v_empty[gvi % C::VST]);
+        if (nxt) umma_commit_by(leader, &k_empty[(gki + 1) % C::KST]);
+        if (t + 2 == it.u1) umma_commit_by(leader, q_empty);  // the item's last S is issued
+      }
+      gk += (uint32_t)(it.u1 - it.u0);
+      gv += (uint32_t)(it.u1 - it.u0);
     }
     umma_commit_by(leader, mma_done);  // every MMA issued above has completed once this fires
     mbar_wait(mma_done, 0, abort_flag, nullptr);
@@ -578,7 +677,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 
 template <int D, bool ALIBI, bool ROPE>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const PrefillParams& p, int max_rows, cudaStream_t stream) {
+                                    const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
   using C = PrefillCfg<D>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static int attr_set[64];
@@ -591,27 +690,32 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  const int rows_per_cta = C::NQT * C::BM;
-  dim3 grid(p.Hq, (max_rows + rows_per_cta - 1) / rows_per_cta, p.B);
-  if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-  fa_prefill_kernel<D, ALIBI, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  // Persistent: one CTA per SM (at most one per item) walks its share of the items.
+  PrefillParams q = p;
+  const int rows_per_item = C::NQT * C::BM;
+  q.n_qblk = (max_rows + rows_per_item - 1) / rows_per_item;
+  const long long n_items = (long long)q.Hq * q.B * q.n_qblk;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items >= (1LL << 31)) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)(n_items < sm_count ? n_items : sm_count);
+  fa_prefill_kernel<D, ALIBI, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t launch_prefill_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                     const PrefillParams& p, int max_rows, cudaStream_t stream) {
+                                     const PrefillParams& p, int max_rows, int sm, cudaStream_t stream) {
   const bool alibi = p.alibi != nullptr, rope = p.rope_cos != nullptr;
-  if (alibi) return rope ? launch_prefill_d<D, true, true>(tq, tk, tv, p, max_rows, stream)
-                         : launch_prefill_d<D, true, false>(tq, tk, tv, p, max_rows, stream);
-  return rope ? launch_prefill_d<D, false, true>(tq, tk, tv, p, max_rows, stream)
-              : launch_prefill_d<D, false, false>(tq, tk, tv, p, max_rows, stream);
+  if (alibi) return rope ? launch_prefill_d<D, true, true>(tq, tk, tv, p, max_rows, sm, stream)
+                         : launch_prefill_d<D, true, false>(tq, tk, tv, p, max_rows, sm, stream);
+  return rope ? launch_prefill_d<D, false, true>(tq, tk, tv, p, max_rows, sm, stream)
+              : launch_prefill_d<D, false, false>(tq, tk, tv, p, max_rows, sm, stream);
 }
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int max_rows, cudaStream_t stream) {
-  return d == 64 ? launch_prefill_dd<64>(tq, tk, tv, p, max_rows, stream)
-                 : launch_prefill_dd<128>(tq, tk, tv, p, max_rows, stream);
+                           const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
+  return d == 64 ? launch_prefill_dd<64>(tq, tk, tv, p, max_rows, sm_count, stream)
+                 : launch_prefill_dd<128>(tq, tk, tv, p, max_rows, sm_count, stream);
 }
 
 int prefill_box_rows() { return PrefillCfg<128>::BM; }
