@@ -298,7 +298,36 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full / p_full phase)
     uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
     uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
+    int rot_k = -1;     // RoPE: the round whose item already has this tile's Q rotated
     bool ok = true;
+    // RoPE: rotate this thread's row of Q_X for item `iq` (bar_q phase `ph`) in place — 16-byte
+    // chunks of the 128-byte swizzled rows the TMA wrote, four adjacent pairs per chunk — and
+    // tell the MMA issuer.  bar_q phases are waited strictly in order (a parity wait more than
+    // one phase ahead would pass early), so a tile with no rows in an item still waits its phase.
+    auto rotate_q = [&](const WorkItem& iq, uint32_t ph) -> bool {
+      const bool good = __all_sync(0xffffffffu, mbar_wait(bar_q, ph & 1, abort_flag, p.err));
+      const QTileRange rq = X ? iq.rb : iq.ra;
+      const int iqr = rq.q0 + rg;
+      if (good && iqr < iq.s.Lq) {
+        const int pos = iqr + iq.s.Lk - iq.s.Lq;
+        if (pos >= 0 && pos < p.rope_rows) {
+          uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
+          const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
+          const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
+          for (int c = 0; c < p.rope_dim / 8; ++c) {
+            uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
+            *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
+                               *reinterpret_cast<const float4*>(st + 4 * c));
+          }
+        } else {
+          atomicOr(p.err, kDevErrBounds);  // no table row for this position
+        }
+      }
+      fence_async_smem();  // the MMA reads Q through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[X]);
+      return good;
+    };
     for (int k = 0; ok && k < n_rounds; ++k) {
       const int w = snake_item(k, n_items);
       if (w < 0) continue;
@@ -310,6 +339,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const int i = r.q0 + rg;
       if (it.u1 > it.u0) ++n_q;
       if (r.t1 <= r.t0) {  // this tile's rows see no key: O = 0, LSE = -inf (and zero padding rows)
+        if (ROPE && it.u1 > it.u0) ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
         if (i < s.rows_out) store_row_zero<D>(p, s, h, i);
         continue;
       }
@@ -320,28 +350,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       float m = -INFINITY;  // running max used for exponentiation (log2 units)
       float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
       float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
-      if (ROPE) {
-        // Rotate this thread's Q row (position pos) in place: 16-byte chunks of the 128-byte
-        // swizzled rows the TMA wrote, four adjacent pairs per chunk.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
-        if (ok && i < s.Lq) {
-          if (pos >= 0 && pos < p.rope_rows) {
-            uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
-            const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
-            const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
-            for (int c = 0; c < p.rope_dim / 8; ++c) {
-              uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
-              *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
-                                 *reinterpret_cast<const float4*>(st + 4 * c));
-            }
-          } else {
-            atomicOr(p.err, kDevErrBounds);  // no table row for this position
-          }
-        }
-        fence_async_smem();  // the MMA reads Q through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_ready[X]);
-      }
+      if (ROPE && rot_k != k) ok = rotate_q(it, n_q - 1);
       for (int t = r.t0; ok && t < r.t1; ++t, ++n_sx) {
         const int n = t - r.t0;
         ok = mbar_wait(&s_full[X], n_sx & 1, abort_flag, p.err);
@@ -378,13 +387,42 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           for (int j = 0; j < C::BN; ++j)
             if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
         }
-        if (ALIBI) {
-          const float dpos = (float)(pos - k0);
-#pragma unroll
-          for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
-        }
+        // ALiBi (bias -m_h |p - j|, log2 units).  When every key of the tile lies on one side of p
+        // — always for causal rows, whose later keys are masked — the bias is linear in the key,
+        // b_j = ba j + bc: it is added inside the exponent's FMA by eight chains of paired adds,
+        // and the row max is bounded per 16-key chunk (scaled raw chunk max plus the chunk's
+        // largest bias).  The bound exceeds the biased max by at most 15 |ba| (below 19 for the
+        // steepest slope), which only lowers every weight of the tile by a common factor, and it
+        // keeps the bias off the max's critical path.  A tile that p splits (non-causal only)
+        // takes |.| per key before the max.
+        bool lin = false;           // ALiBi bias added in the exponent
+        float ba = 0.f, bc = 0.f;   // b_j = ba j + bc (log2 units)
+        float xs_t = xs;            // scale applied in the exponent's FMA
         float mx;
-        {  // row max: eight independent chains of three-input max
+        if (ALIBI) {
+          const int dk = pos - k0;
+          lin = p.causal || dk >= C::BN - 1 || dk <= 0;
+          if (lin) {
+            ba = (p.causal || dk > 0) ? slope2 : -slope2;
+            bc = -ba * (float)dk;
+            xs_t = sl2;
+            const float jtop = ba >= 0.f ? 15.f : 0.f;  // key of a chunk's largest bias
+            float c8[C::BN / 16];
+#pragma unroll
+            for (int q = 0; q < C::BN / 16; ++q) {
+              const float* v = sc + 16 * q;
+              const float c16 = fmax3(fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmax3(v[6], v[7], v[8])),
+                                      fmax3(v[9], v[10], v[11]), fmax3(fmax3(v[12], v[13], v[14]), v[15], v[15]));
+              c8[q] = fmaf(c16, sl2, fmaf(ba, (float)(16 * q) + jtop, bc));
+            }
+            mx = fmax3(fmax3(c8[0], c8[1], c8[2]), fmax3(c8[3], c8[4], c8[5]), fmaxf(c8[6], c8[7]));
+          } else {
+            const float dpos = (float)dk;
+#pragma unroll
+            for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
+          }
+        }
+        if (!lin) {  // row max: eight independent chains of three-input max
           float t8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
@@ -394,9 +432,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             for (int u = 0; u < 8; ++u) t8[u] = fmax3(t8[u], sc[j + u], sc[j + 8 + u]);
 #pragma unroll
           for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
-          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7])) * xs;
         }
-        mx *= xs;
         const float m_new = fmaxf(m, mx);
         const bool need = m_new > m + 8.0f;  // -inf + 8 = -inf: the first finite max always moves m
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
@@ -424,7 +461,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
         // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
         // (two accumulators each to keep the dependency chains short).
-        const uint64_t sl2x2 = f2_pack(xs, xs), negm2 = f2_pack(-m_use, -m_use);
+        const uint64_t sl2x2 = f2_pack(xs_t, xs_t), negm2 = f2_pack(-m_use, -m_use);
+        // ALiBi: exponent addend b_j - m per key pair, eight chains stepping 16 keys
+        uint64_t bm[8];
+        const uint64_t bstep = f2_pack(16.f * ba, 16.f * ba);
+        if (ALIBI) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            bm[u] = f2_pack(fmaf(ba, (float)(2 * u), bc) - m_use, fmaf(ba, (float)(2 * u + 1), bc) - m_use);
+        }
         uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
         float lr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -433,7 +478,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float x0, x1;
-            f2_unpack(f2_fma(f2_pack(sc[32 * c + 2 * j], sc[32 * c + 2 * j + 1]), sl2x2, negm2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(sc[32 * c + 2 * j], sc[32 * c + 2 * j + 1]), sl2x2, ALIBI ? bm[j & 7] : negm2),
+                      x0, x1);
+            if (ALIBI) bm[j & 7] = f2_add(bm[j & 7], bstep);
             const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
             ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
             pk[j] = pack_bf16x2(e0, e1);
@@ -451,6 +498,23 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[X]);
+      }
+      if (ROPE && ok) {
+        // Look ahead: when the next item with any work has rows in this tile, rotate its Q now
+        // (it lands once this item's last S has run), so the next item's first S can run while
+        // this item's epilogue does.
+        for (int k2 = k + 1; k2 < n_rounds; ++k2) {
+          const int w2 = snake_item(k2, n_items);
+          if (w2 < 0) continue;
+          const WorkItem it2 = work_item<C::BM, C::BN>(p, w2);
+          if (!it2.live || it2.u1 <= it2.u0) continue;
+          const QTileRange r2 = X ? it2.rb : it2.ra;
+          if (r2.t1 > r2.t0) {
+            ok = rotate_q(it2, n_q);
+            rot_k = k2;
+          }
+          break;
+        }
       }
       if (ok) {
         ok = mbar_wait(&o_final[X], n_ox & 1, abort_flag, p.err);  // the last PV of this tile finished
@@ -690,14 +754,17 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  // Persistent: one CTA per SM (at most one per item) walks its share of the items.
+  // Persistent (one CTA per SM walks its share of the items) when every sequence has the same
+  // lengths, so that the static order balances; with per-sequence lengths the item costs are
+  // unknown here, and one CTA per item lets the hardware scheduler balance them.
   PrefillParams q = p;
   const int rows_per_item = C::NQT * C::BM;
   q.n_qblk = (max_rows + rows_per_item - 1) / rows_per_item;
   const long long n_items = (long long)q.Hq * q.B * q.n_qblk;
   if (n_items <= 0) return cudaSuccess;
   if (n_items >= (1LL << 31)) return cudaErrorInvalidConfiguration;
-  const unsigned grid = (unsigned)(n_items < sm_count ? n_items : sm_count);
+  const bool uniform = !p.cu_q && !p.seqlens_q && !p.seqlens_k;
+  const unsigned grid = (unsigned)(uniform && n_items > sm_count ? sm_count : n_items);
   fa_prefill_kernel<D, ALIBI, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
