@@ -38,8 +38,11 @@
 //   own Q row in shared memory right after the TMA load, before the first S_X; K arrives
 //   rotated (a K tile is read by every CTA of its head, so it is rotated once, not per CTA).
 //   Each Q tile visits only the K/V tiles its rows can see (causal / window
-//   tiles that are fully masked are never loaded or multiplied); only tiles
-//   crossing a mask edge or the ragged tail evaluate the mask.
+//   tiles that are fully masked are never loaded or multiplied).  With ALiBi
+//   the walk starts at the last tile: the diagonal, where ALiBi scores peak,
+//   sets the running max early, so later tiles rarely move it and O is rarely
+//   rescaled; otherwise it starts at the first, so the CTAs of one head stream
+//   the same early K/V tiles at about the same time and share them in L2.  Only tiles crossing a mask edge or the ragged tail evaluate the mask.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = p.Hq * p.B * p.n_qblk;
   const int n_rounds = (int)(((long long)n_items + gridDim.x - 1) / gridDim.x);
+  constexpr bool rev = ALIBI;  // walk each item's K/V tiles last to first
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,8 +355,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
       float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
       if (ROPE && rot_k != k) ok = rotate_q(it, n_q - 1);
-      for (int t = r.t0; ok && t < r.t1; ++t, ++n_sx) {
-        const int n = t - r.t0;
+      for (int t = rev ? r.t1 - 1 : r.t0; ok && (rev ? t >= r.t0 : t < r.t1); t += rev ? -1 : 1, ++n_sx) {
+        const int n = rev ? r.t1 - 1 - t : t - r.t0;  // position of tile t in the walk
         ok = mbar_wait(&s_full[X], n_sx & 1, abort_flag, p.err);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
                         it.s.q_row0 + it.q0 + X * C::BM);
         ++n_q;
         const int hkv = it.h / p.group;
-        for (int t = it.u0; t < it.u1; ++t, ++gk) {
+        for (int t = rev ? it.u1 - 1 : it.u0; rev ? t >= it.u0 : t < it.u1; t += rev ? -1 : 1, ++gk) {
           const uint32_t st = gk % C::KST;
           if (gk >= (uint32_t)C::KST && !mbar_wait(&k_empty[st], ((gk / C::KST) + 1) & 1, abort_flag, p.err)) {
             ok = false;
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const WorkItem it = work_item<C::BM, C::BN>(p, w);
         if (!it.live || it.u1 <= it.u0) continue;
         const int hkv = it.h / p.group;
-        for (int t = it.u0; t < it.u1; ++t, ++gv) {
+        for (int t = rev ? it.u1 - 1 : it.u0; rev ? t >= it.u0 : t < it.u1; t += rev ? -1 : 1, ++gv) {
           const uint32_t st = gv % C::VST;
           if (gv >= (uint32_t)C::VST && !mbar_wait(&v_empty[st], ((gv / C::VST) + 1) & 1, abort_flag, p.err)) {
             ok = false;
@@ -653,12 +657,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const uint64_t vd = v_desc + (uint64_t)(((g % C::VST) * C::KV_BYTES) >> 4);
       const uint32_t p_cols = tmem + C::COL_S + 128u * X;
       const uint32_t d_cols = tmem + C::COL_O + (uint32_t)D * X;
-      const uint32_t acc0 = t > r.t0 ? 1u : 0u;
+      const uint32_t acc0 = (rev ? t < r.t1 - 1 : t > r.t0) ? 1u : 0u;  // the walk's first P V overwrites O_X
 #pragma unroll
       for (int kk = 0; kk < C::BN / 16; ++kk)
         umma_ts_by(leader, d_cols, p_cols + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_O,
                    kk > 0 ? 1u : acc0);
-      if (t == r.t1 - 1) umma_commit_by(leader, &o_final[X]);
+      if (t == (rev ? r.t0 : r.t1 - 1)) umma_commit_by(leader, &o_final[X]);
     };
     uint32_t gk = 0, gv = 0;              // K / V tiles consumed (ring indices)
     uint32_t n_q = 0;                     // items (bar_q phase)
@@ -683,13 +687,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      if (act_a && it.ra.t0 == it.u0) issue_s(0, gk);
-      if (act_b && it.rb.t0 == it.u0) issue_s(1, gk);
+      if (act_a && (rev ? it.ra.t1 == it.u1 : it.ra.t0 == it.u0)) issue_s(0, gk);
+      if (act_b && (rev ? it.rb.t1 == it.u1 : it.rb.t0 == it.u0)) issue_s(1, gk);
       umma_commit_by(leader, &k_empty[gk % C::KST]);
       if (it.u1 - it.u0 == 1) umma_commit_by(leader, q_empty);  // every S of the item is issued
-      for (int t = it.u0; ok && t < it.u1; ++t) {
-        const uint32_t gki = gk + (uint32_t)(t - it.u0), gvi = gv + (uint32_t)(t - it.u0);
-        const bool nxt = t + 1 < it.u1;
+      for (int t = rev ? it.u1 - 1 : it.u0; ok && (rev ? t >= it.u0 : t < it.u1); t += rev ? -1 : 1) {
+        const int j = rev ? it.u1 - 1 - t : t - it.u0;  // position of tile t in the walk
+        const int tn = rev ? t - 1 : t + 1;             // the next tile of the walk
+        const uint32_t gki = gk + (uint32_t)j, gvi = gv + (uint32_t)j;
+        const bool nxt = rev ? tn >= it.u0 : tn < it.u1;
         bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int X = 0; X < C::NQT; ++X) {
@@ -706,7 +712,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             tc_fence_after();
             issue_pv(X, t, gvi, r);
           }
-          if (nxt && t + 1 >= r.t0 && t + 1 < r.t1) {
+          if (nxt && tn >= r.t0 && tn < r.t1) {
             if (!k_ready) {
               ok = __all_sync(0xffffffffu, mbar_wait(&k_full[(gki + 1) % C::KST], ((gki + 1) / C::KST) & 1,
                                                      abort_flag, p.err));
@@ -720,7 +726,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         if (!ok) break;
         umma_commit_by(leader, &v_empty[gvi % C::VST]);
         if (nxt) umma_commit_by(leader, &k_empty[(gki + 1) % C::KST]);
-        if (t + 2 == it.u1) umma_commit_by(leader, q_empty);  // the item's last S is issued
+        if (rev ? tn == it.u0 : tn == it.u1 - 1) umma_commit_by(leader, q_empty);  // the item's last S is issued
       }
       gk += (uint32_t)(it.u1 - it.u0);
       gv += (uint32_t)(it.u1 - it.u0);
