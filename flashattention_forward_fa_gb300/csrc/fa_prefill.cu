@@ -225,6 +225,60 @@ __device__ __forceinline__ int snake_item(int k, int n_items) {
   return w < n_items ? (int)w : -1;
 }
 
+// RoPE: rotate Q_X of item `iq` in place once its Q has landed (bar_q phase `ph`) — 16-byte
+// chunks of the 128-byte swizzled rows the TMA wrote, four adjacent pairs per chunk — and tell the
+// MMA issuer (q_ready[X]).  Warp w of the warpgroup takes rows 32 (w & 3) .. 32 (w & 3) + 31, two
+// per step: lanes 0-15 the chunks of one row, lanes 16-31 those of the next, so that a warp's
+// table load reads 512 contiguous bytes (a table row holds rope_dim / 8 float4 of cos, the same of
+// sin).  Four steps' loads are issued before their stores (Q is reached through a generic pointer,
+// so the compiler never moves a load above an earlier store); a lane with nothing to rotate loads
+// table entry 0 and stores nothing.  Returns false if the wait gave up.
+template <int D>
+__device__ __forceinline__ bool rotate_q_tile(const PrefillParams& p, const WorkItem& iq, uint32_t ph, int X, int warp,
+                                              int lane, uint8_t* sQ, uint64_t* bar_q, uint64_t* q_ready,
+                                              volatile int* abort_flag) {
+  using C = PrefillCfg<D>;
+  const bool good = __all_sync(0xffffffffu, mbar_wait(bar_q, ph & 1, abort_flag, p.err));
+  if (good) {
+    const QTileRange rq = X ? iq.rb : iq.ra;
+    const int nch = p.rope_dim / 8;  // chunks per row to rotate (at most D / 8 <= 16)
+    const int c = lane & 15;
+    const int shift = iq.s.Lk - iq.s.Lq;
+    const float4* cos4 = reinterpret_cast<const float4*>(p.rope_cos);
+    const float4* sin4 = reinterpret_cast<const float4*>(p.rope_sin);
+    uint8_t* qt = sQ + X * C::Q_BYTES;
+#pragma unroll 1
+    for (int kb = 0; kb < 16; kb += 4) {
+      float4 cv[4], sv[4];
+      uint32_t qoff[4];
+      uint32_t live = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = (warp & 3) * 32 + 2 * (kb + u) + (lane >> 4);  // row within the tile
+        const int i = rq.q0 + row, pos = i + shift;
+        const bool in = c < nch && i < iq.s.Lq;
+        const bool okp = in && pos >= 0 && pos < p.rope_rows;
+        if (in && !okp) atomicOr(p.err, kDevErrBounds);  // no table row for this position
+        const size_t tix = okp ? (size_t)pos * nch + c : 0;
+        cv[u] = __ldg(cos4 + tix);
+        sv[u] = __ldg(sin4 + tix);
+        qoff[u] = (uint32_t)((c >> 3) * C::CHUNK + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+        live |= (okp ? 1u : 0u) << u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if ((live >> u) & 1u) {
+          uint4* ch = reinterpret_cast<uint4*>(qt + qoff[u]);
+          *ch = rope_rotate4(*ch, cv[u], sv[u]);
+        }
+    }
+  }
+  fence_async_smem();  // the MMA reads Q through the async proxy
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&q_ready[X]);
+  return good;
+}
+
 template <int D, bool ALIBI, bool ROPE>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -304,33 +358,11 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
     int rot_k = -1;     // RoPE: the round whose item already has this tile's Q rotated
     bool ok = true;
-    // RoPE: rotate this thread's row of Q_X for item `iq` (bar_q phase `ph`) in place — 16-byte
-    // chunks of the 128-byte swizzled rows the TMA wrote, four adjacent pairs per chunk — and
-    // tell the MMA issuer.  bar_q phases are waited strictly in order (a parity wait more than
-    // one phase ahead would pass early), so a tile with no rows in an item still waits its phase.
+    // RoPE rotation of Q_X (rotate_q_tile).  bar_q phases are waited strictly in order (a parity
+    // wait more than one phase ahead would pass early), so a tile with no rows in an item still
+    // waits its phase.
     auto rotate_q = [&](const WorkItem& iq, uint32_t ph) -> bool {
-      const bool good = __all_sync(0xffffffffu, mbar_wait(bar_q, ph & 1, abort_flag, p.err));
-      const QTileRange rq = X ? iq.rb : iq.ra;
-      const int iqr = rq.q0 + rg;
-      if (good && iqr < iq.s.Lq) {
-        const int pos = iqr + iq.s.Lk - iq.s.Lq;
-        if (pos >= 0 && pos < p.rope_rows) {
-          uint8_t* qrow = sQ + X * C::Q_BYTES + rg * 128;
-          const float* ct = p.rope_cos + (size_t)pos * (p.rope_dim / 2);
-          const float* st = p.rope_sin + (size_t)pos * (p.rope_dim / 2);
-          for (int c = 0; c < p.rope_dim / 8; ++c) {
-            uint4* ch = reinterpret_cast<uint4*>(qrow + (c >> 3) * C::CHUNK + (((c & 7) ^ (rg & 7)) << 4));
-            *ch = rope_rotate4(*ch, *reinterpret_cast<const float4*>(ct + 4 * c),
-                               *reinterpret_cast<const float4*>(st + 4 * c));
-          }
-        } else {
-          atomicOr(p.err, kDevErrBounds);  // no table row for this position
-        }
-      }
-      fence_async_smem();  // the MMA reads Q through the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_ready[X]);
-      return good;
+      return rotate_q_tile<D>(p, iq, ph, X, warp, lane, sQ, bar_q, q_ready, abort_flag);
     };
     for (int k = 0; ok && k < n_rounds; ++k) {
       const int w = snake_item(k, n_items);

@@ -78,6 +78,7 @@ def _oracle_rope_prefill(x, case, cos64, sin64, rd):
     (PrefillCase("rope_window", B=1, Hq=8, Hkv=2, Nq=600, Nk=600, d=128, causal=True, window=200, seed=504), 64),
     (PrefillCase("rope_varlen", B=3, Hq=4, Hkv=4, Nq=500, Nk=500, d=64, layout="packed", causal=True,
                  len_q=[500, 17, 256], seed=505), 64),
+    (PrefillCase("rope_dim40_tail", B=1, Hq=4, Hkv=4, Nq=384, Nk=384, d=128, causal=True, seed=508), 40),
 ], ids=lambda c: c.name if hasattr(c, "name") else str(c))
 def test_fused_rope_prefill_matches_oracle(case, rd):
     import flashattention_forward_fa_gb300 as fa
