@@ -404,11 +404,12 @@ def gpu_arm(args, world, rank, local):
 
 
 def single_kernel_run(args, dev, stream):
-    """--only prefill|decode: warm-up then ``steps`` launches of one phase of the step, nothing else
-    (no e2e, no CPU baseline, no clock sampling).  Used as the command under ncu."""
+    """--only prefill|window|decode: warm-up then ``steps`` launches of one kernel workload
+    (llama7b_causal, gqa_window or decode_cache), nothing else (no e2e, no CPU baseline, no clock
+    sampling).  Used as the command under ncu."""
     import flashattention_forward_fa_gb300 as fa
-    if args.only == "prefill":
-        pc = LLAMA7B_CAUSAL
+    if args.only in ("prefill", "window"):
+        pc = LLAMA7B_CAUSAL if args.only == "prefill" else GQA_WINDOW
         px = make_prefill(pc)
         q, k, v = px.q.to(dev), px.k.to(dev), px.v.to(dev)
         o = torch.empty_like(q)
@@ -604,7 +605,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "window", "decode"], default=None,
                     help="run one phase alone (for profilers); prints a partial line")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the per-workload rows (other workloads and option paths) after the step")

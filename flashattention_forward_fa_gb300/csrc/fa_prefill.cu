@@ -609,6 +609,27 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
                         it.s.q_row0 + it.q0 + X * C::BM);
         ++n_q;
         const int hkv = it.h / p.group;
+        // Bring the next item's Q and first K tiles into L2 now: its Q load can only start once
+        // this item's last S has run, and then hits L2 instead of HBM.  (With RoPE the next Q is
+        // waited for by the softmax warps themselves and the prefetch measured slower.)
+        for (int k2 = k + 1; !ROPE && k2 < n_rounds; ++k2) {
+          const int w2 = snake_item(k2, n_items);
+          if (w2 < 0) continue;
+          const WorkItem nx = work_item<C::BM, C::BN>(p, w2);
+          if (!nx.live || nx.u1 <= nx.u0) continue;
+#pragma unroll
+          for (int X = 0; X < C::NQT; ++X)
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_prefetch_l2_3d(&tm_q, c * 64, nx.h, nx.s.q_row0 + nx.q0 + X * C::BM);
+          for (int j = 0; j < C::KST && j < nx.u1 - nx.u0; ++j) {
+            const int t2 = rev ? nx.u1 - 1 - j : nx.u0 + j;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_prefetch_l2_3d(&tm_k, c * 64, nx.h / p.group, nx.s.k_row0 + t2 * C::BN);
+          }
+          break;
+        }
         for (int t = rev ? it.u1 - 1 : it.u0; rev ? t >= it.u0 : t < it.u1; t += rev ? -1 : 1, ++gk) {
           const uint32_t st = gk % C::KST;
           if (gk >= (uint32_t)C::KST && !mbar_wait(&k_empty[st], ((gk / C::KST) + 1) & 1, abort_flag, p.err)) {
