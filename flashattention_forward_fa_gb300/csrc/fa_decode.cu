@@ -380,8 +380,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
 
 // One warp per (sequence, new token, query head): merge the chunk partials.  O is
 // [B, nq, Hq, d]; LSE is [B, Hq, nq].
+// Launched as a programmatic dependent of the split kernel: it may start while the split kernel
+// drains and waits here until the split kernel's partials are complete and visible.
 template <int D>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.B * p.nq * p.Hq) return;
@@ -412,7 +415,8 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
 #pragma unroll
   for (int j = 0; j < PER; ++j) acc[j] = 0.f;
   float tot = 0.f;
-  for (int s = 0; s < ns; ++s) {
+#pragma unroll 4
+  for (int s = 0; s < ns; ++s) {  // unrolled: several partials' loads in flight
     const float w = ex2_approx((p.lse_part[prow0 + s] - mx) * LOG2E);
     tot += w;
     const float* op = p.o_part + (prow0 + s) * D + lane * PER;
@@ -459,8 +463,17 @@ static cudaError_t launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv,
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = p.B * p.nq * p.Hq;
-  fa_decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the launch with the split's tail
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D>, p);
 }
 
 template <int D>
