@@ -17,6 +17,7 @@ Entry points (same names as the C ABI):
 * ``fa_fwd_ex`` / ``fa_decode_ex`` (C ABI): every option in one struct; reached from
   the wrappers above when ``alibi_slopes`` or ``rope`` is given
 * ``fa_device_status()``           read/clear the kernels' error word
+* ``fa_selftest_wait_timeout()``   a wait that runs out on purpose, ending with the timeout bit
 """
 
 from __future__ import annotations
@@ -35,6 +36,7 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_varlen,
     fa_rope,
+    fa_selftest_wait_timeout,
     library_path,
     load_library,
     rope_tables,
@@ -55,6 +57,7 @@ __all__ = [
     "fa_decode_paged",
     "decode_workspace_size",
     "fa_device_status",
+    "fa_selftest_wait_timeout",
     "load_library",
     "library_path",
 ]

@@ -53,6 +53,7 @@ _SIGS = {
     "fa_decode_ex": (_i, [ctypes.POINTER(DecodeArgs), _vp]),
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
     "fa_rope": (_i, [_vp, ctypes.c_longlong, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
+    "fa_selftest_wait_timeout": (_i, [_i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
 }
@@ -402,6 +403,13 @@ def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                  sc, int(window), _ptr(seqlens_k), ctypes.cast(host, _ip) if host is not None else None,
                                  int(num_splits), _stream(q)))
     return o, lse
+
+
+def fa_selftest_wait_timeout(limit_ms: int = 20, stream=None) -> None:
+    """Launch the library's wait self-test (a wait that nothing completes, limited to limit_ms);
+    afterwards fa_device_status() shows the timeout bit (1)."""
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    _check(load_library().fa_selftest_wait_timeout(int(limit_ms), ctypes.c_void_p(s)))
 
 
 def fa_device_status(clear: bool = True) -> int:

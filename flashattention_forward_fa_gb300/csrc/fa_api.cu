@@ -13,6 +13,7 @@
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -518,6 +519,34 @@ fa_status fa_rope(void* x, long long rows, int heads, int d, int rotary_dim, con
   p.err = di->status;
   cudaError_t e = fa::launch_rope(p, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+  return FA_OK;
+}
+
+namespace fa {
+// One warp waits on an mbarrier that nothing arrives at, through the same bounded wait every
+// kernel uses, with a short limit: the wait must end with the timeout bit in the status word.
+__global__ void fa_selftest_wait_kernel(uint32_t* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+}
+}  // namespace fa
+
+fa_status fa_selftest_wait_timeout(int limit_ms, fa_stream_t stream) {
+  if (limit_ms <= 0 || limit_ms > 1000) return fail(FA_ERR_INVALID, "limit_ms must be in 1..1000");
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(&di);
+  if (st != FA_OK) return st;
+  fa::fa_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      di->status, (unsigned long long)limit_ms * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return FA_OK;
 }
 

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::THREADS)
       }
       for (int st = 0; st < C::ST && st < t; ++st) {  // drain: all issued loads have landed
         const int last = st + ((t - 1 - st) / C::ST) * C::ST;
-        mbar_wait(&full[st], (last / C::ST) & 1, abort_flag, nullptr);
+        mbar_wait_drain(&full[st], (last / C::ST) & 1);
       }
     }
     return;  // the producer takes no part in the merge below

@@ -644,10 +644,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
       }
       // drain: every issued load has landed before the CTA may exit
-      if (n_q > 0) mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, nullptr);
+      if (n_q > 0) mbar_wait_drain(bar_q, (n_q - 1) & 1);
       for (uint32_t st = 0; st < (uint32_t)C::KST && st < gk; ++st) {
         const uint32_t last = st + ((gk - 1 - st) / C::KST) * C::KST;
-        mbar_wait(&k_full[st], (last / C::KST) & 1, abort_flag, nullptr);
+        mbar_wait_drain(&k_full[st], (last / C::KST) & 1);
       }
     }
   } else if (warp == 9) {
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
       for (uint32_t st = 0; st < (uint32_t)C::VST && st < gv; ++st) {
         const uint32_t last = st + ((gv - 1 - st) / C::VST) * C::VST;
-        mbar_wait(&v_full[st], (last / C::VST) & 1, abort_flag, nullptr);
+        mbar_wait_drain(&v_full[st], (last / C::VST) & 1);
       }
     }
   } else if (warp == 10) {
@@ -785,7 +785,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       gv += (uint32_t)(it.u1 - it.u0);
     }
     umma_commit_by(leader, mma_done);  // every MMA issued above has completed once this fires
-    mbar_wait(mma_done, 0, abort_flag, nullptr);
+    mbar_wait_drain(mma_done, 0);
     __syncwarp();
   } else {
     setmaxnreg_dec<C::REGS_PRODUCER>();  // warp 11: idle, its registers go to the softmax warps

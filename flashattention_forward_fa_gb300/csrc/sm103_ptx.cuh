@@ -69,7 +69,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // sets *abort and the device error word) when the time limit passes or when
 // another thread of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* dev_err) {
+                                          uint32_t* dev_err, uint64_t limit_ns = FA_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
@@ -77,12 +77,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > FA_WAIT_LIMIT_NS) {
+    if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       if (dev_err) atomicOr(dev_err, kDevErrTimeout);
       return false;
     }
   }
+}
+
+// Wait for this CTA's own asynchronous work (TMA loads, MMAs) to finish before it exits or frees
+// TMEM: unlike mbar_wait it does not give up when another role has aborted, only after the same
+// time limit, so an abort never leaves a copy or an MMA writing into released memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 <= FA_WAIT_LIMIT_NS) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
 }
 
 // ------------------------------------------------------------------ TMA

@@ -289,6 +289,15 @@ FA_API fa_status fa_decode_noalloc(const void* q, const void* k_cache, const voi
 FA_API const char* fa_last_error(void);
 
 /*
+ * Diagnostic: launch one warp that waits on a barrier nothing arrives at, through the same
+ * bounded wait as every kernel, with a limit of limit_ms (1..1000) milliseconds.  The wait ends,
+ * sets bit 0 of the device status word (fa_device_status) and the kernel returns: the check that
+ * a wait which never completes ends with an error status, and leaves the context usable, instead
+ * of hanging the GPU.  Asynchronous on `stream`; FA_ERR_INVALID for a limit out of range.
+ */
+FA_API fa_status fa_selftest_wait_timeout(int limit_ms, fa_stream_t stream);
+
+/*
  * Read (and optionally clear) the device status word of the current device:
  * bit 0 = some kernel wait passed its time limit, bit 1 = a device-side bounds
  * check fired.  Synchronises the device.  Returns FA_ERR_TIMEOUT when bits

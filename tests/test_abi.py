@@ -225,3 +225,10 @@ def test_rope_tables_match_oracle_tables():
     assert c.dtype.is_floating_point and tuple(c.shape) == (300, 32)
     np.testing.assert_allclose(c.numpy(), rc, atol=1e-7)
     np.testing.assert_allclose(s.numpy(), rs, atol=1e-7)
+
+
+def test_selftest_wait_timeout_arguments_checked(lib):
+    _, b = _binding()
+    L = b.load_library()
+    assert L.fa_selftest_wait_timeout(0, None) == 1
+    assert L.fa_selftest_wait_timeout(5000, None) == 1 and b"limit_ms" in L.fa_last_error()
