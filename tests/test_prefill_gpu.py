@@ -55,6 +55,26 @@ def test_full_size_sampled(case):
     assert fa.fa_device_status() == 0
 
 
+@pytest.mark.parametrize("case", [
+    # one long MQA sequence: 128 items, each walking up to 256 K/V tiles
+    PrefillCase("long_context_32k_mqa", B=1, Hq=4, Hkv=1, Nq=32768, Nk=32768, d=128, causal=True, seed=21),
+    # d=64 GQA with a ragged tail: 384 items, three snake rounds per resident CTA
+    PrefillCase("d64_gqa_three_rounds", B=2, Hq=16, Hkv=4, Nq=3000, Nk=3000, d=64, causal=True, seed=22),
+    # non-causal at the persistent grid: every item walks every K/V tile
+    PrefillCase("noncausal_persistent", B=3, Hq=24, Hkv=8, Nq=1100, Nk=1700, d=128, seed=23),
+], ids=lambda c: c.name)
+def test_persistent_schedules_sampled(case):
+    x = make_prefill(case)
+    o, lse = gpu_prefill(x)
+    rows = sample_rows(x, per_head=16, seed=case.seed)
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    ro, rl = oracle_prefill_rows(x, rows)
+    check(go, gl, ro, rl, case.name)
+    assert torch.isfinite(o.float()).all()
+    import flashattention_forward_fa_gb300 as fa
+    assert fa.fa_device_status() == 0
+
+
 # ------------------------------------------------------------------ reduced-size families
 
 @pytest.mark.parametrize("case", [
