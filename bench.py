@@ -507,7 +507,7 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
         rows[name] = {"workload": workload, "ms": round(ms, 4), "value": round(val, 2), "unit": unit,
                       "bound": bound, "frac": round(val / peak, 4), "inputs_vs_l2": l2}
 
-    def prefill_row(name, case, desc, l2, **kw):
+    def prefill_row(name, case, desc, l2, graph=False, **kw):
         x = make_prefill(case)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
         if case.layout == "packed":
@@ -518,11 +518,23 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
         else:
             fn = lambda: fa.fa_fwd(q, k, v, causal=case.causal, window=case.window,  # noqa: E731
                                    scale=case.softmax_scale, **kw)
-        add(name, desc, time_alone(fn, steps, warm, stream), prefill_flops(case, x.len_q, x.len_k), "TFLOP/s",
-            "tensor", l2)
+        work = prefill_flops(case, x.len_q, x.len_k)
+        add(name, desc, time_alone(fn, steps, warm, stream), work, "TFLOP/s", "tensor", l2)
+        if graph:  # launch-bound: also replay the call from a captured CUDA graph (no host work per call)
+            reps = 20
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            (gms,), _ = time_steps([g.replay], max(3, steps // reps), stream)
+            rows[name]["graph_ms_per_call"] = round(gms / reps, 5)
+            rows[name]["graph_value"] = round(work / (gms / reps * 1e-3) / 1e12, 2)
 
-    prefill_row("tiny_mha", TINY_MHA, "B=1, H=2, N=256, d=64, non-causal (launch-bound)", "inside L2")
-    prefill_row("bert_varlen", BERT_VARLEN, "B=8, H=12, d=64, len U[128,512] packed, non-causal", "inside L2")
+    prefill_row("tiny_mha", TINY_MHA, "B=1, H=2, N=256, d=64, non-causal (launch-bound)", "inside L2", graph=True)
+    prefill_row("bert_varlen", BERT_VARLEN, "B=8, H=12, d=64, len U[128,512] packed, non-causal", "inside L2",
+                graph=True)
     prefill_row("gqa_window", GQA_WINDOW, "B=4, Hq=32, Hkv=8, N=4096, d=128, causal, window 1024",
                 "larger than L2 (320 MB)")
 
@@ -550,7 +562,20 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
                     steps, warm, stream)
     add("rope_prefill", "llama7b_causal, Q rotated in the kernel (rotary_dim 128)", ms, flops, "TFLOP/s", "tensor",
         "larger than L2")
-    del kr
+    # the same work in two passes, for comparison: Q rotated in place by fa_rope (as a model would rotate
+    # its fresh Q projection; a copy is rotated again each time, which changes no cost), then the
+    # plain kernel
+    qr = q.clone()
+    qpos = torch.arange(pc.Nq, dtype=torch.int32, device=dev).repeat(pc.B)
+
+    def two_pass():
+        fa.fa_rope(qr, qpos, (cos_t, sin_t))
+        fa.fa_fwd(qr, kr, v, causal=True, scale=pc.softmax_scale, out=o)
+
+    ms = time_alone(two_pass, steps, warm, stream)
+    add("rope_prefill_two_pass", "the same work in two launches: fa_rope on Q in place, then the plain kernel",
+        ms, flops, "TFLOP/s", "tensor", "larger than L2")
+    del kr, qr
     # ... and the in-place rotation pass itself over a 256 MB K block (4 x 8192 rows)
     xr = torch.randn(4 * pc.Nk, pc.Hkv, pc.d, device=dev).to(torch.bfloat16)
     pos = torch.arange(pc.Nk, dtype=torch.int32, device=dev).repeat(4)
