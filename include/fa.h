@@ -257,7 +257,7 @@ FA_API fa_status fa_decode_ex(const fa_decode_args* args, fa_stream_t stream);
 FA_API int fa_decode_max_splits(int B, int Hq, int Hkv, int Ncap, int window, const int* seqlens_k_host, int num_splits);
 
 /*
- * fa_decode without any device allocation.  The paper has no counterpart: this
+ * fa_decode without any device allocation.  The attention pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc — for example a
  * plugin inside an inference engine that is handed only its input and output
  * buffers, or a serving loop that must not take the allocator's locks or the
