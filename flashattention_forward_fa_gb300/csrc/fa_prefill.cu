@@ -279,7 +279,9 @@ __device__ __forceinline__ bool rotate_q_tile(const PrefillParams& p, const Work
   return good;
 }
 
-template <int D, bool ALIBI, bool ROPE>
+// PADK: padded layout with per-sequence key lengths, where K/V rows past a sequence's keys are
+// in-bounds caller memory (see the zeroing of V below); other layouts compile without that code.
+template <int D, bool ALIBI, bool ROPE, bool PADK>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full / p_full phase)
     uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
     uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
+    uint32_t v_next = 0;  // V ring index of the next item's first tile
     int rot_k = -1;     // RoPE: the round whose item already has this tile's Q rotated
     bool ok = true;
     // RoPE rotation of Q_X (rotate_q_tile).  bar_q phases are waited strictly in order (a parity
@@ -374,6 +377,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const int h = it.h;
       const int i = r.q0 + rg;
       if (it.u1 > it.u0) ++n_q;
+      const uint32_t v_first = v_next;  // V ring index of this item's first tile
+      if (it.u1 > it.u0) v_next += (uint32_t)(it.u1 - it.u0);
       if (r.t1 <= r.t0) {  // this tile's rows see no key: O = 0, LSE = -inf (and zero padding rows)
         if (ROPE && it.u1 > it.u0) ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
         if (i < s.rows_out) store_row_zero<D>(p, s, h, i);
@@ -422,6 +427,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < C::BN; ++j)
             if ((uint32_t)j - lo >= span) sc[j] = -INFINITY;
+          if (PADK && k0 + C::BN > s.Lk) {
+            // The tile crosses the end of the sequence's keys: the V rows past it are in-bounds
+            // memory the caller may leave as anything, and 0 * NaN is NaN in P V.  Zero them (whole
+            // 128-byte rows of each slab, so the swizzle does not matter) once V has landed; the
+            // p_full arrival below orders this before the first P V that reads the tile.  Both
+            // warpgroups may do it for the same tile; writing zeros over zeros changes nothing.
+            const uint32_t g = v_first + (uint32_t)(rev ? it.u1 - 1 - t : t - it.u0);
+            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[g % C::VST], (g / C::VST) & 1, abort_flag, p.err));
+            if (ok) {
+              uint8_t* vt = sV + (g % C::VST) * C::KV_BYTES;
+              const int nvalid = s.Lk - k0;
+              for (int idx = rg; idx < (C::BN - nvalid) * (D / 8); idx += 128) {
+                const int row = nvalid + idx / (D / 8), c16 = idx % (D / 8);
+                *reinterpret_cast<uint4*>(vt + (c16 >> 3) * C::CHUNK + row * 128 + ((c16 & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_async_smem();  // the MMA reads V through the async proxy
+            }
+          }
         }
         // ALiBi (bias -m_h |p - j|, log2 units).  When every key of the tile lies on one side of p
         // — always for causal rows, whose later keys are masked — the bias is linear in the key,
@@ -798,7 +822,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool ALIBI, bool ROPE>
+template <int D, bool ALIBI, bool ROPE, bool PADK>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
   using C = PrefillCfg<D>;
@@ -808,7 +832,7 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI, ROPE, PADK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
@@ -824,18 +848,26 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   if (n_items >= (1LL << 31)) return cudaErrorInvalidConfiguration;
   const bool uniform = !p.cu_q && !p.seqlens_q && !p.seqlens_k;
   const unsigned grid = (unsigned)(uniform && n_items > sm_count ? sm_count : n_items);
-  fa_prefill_kernel<D, ALIBI, ROPE><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, q);
+  fa_prefill_kernel<D, ALIBI, ROPE, PADK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
+}
+
+template <int D, bool ALIBI, bool ROPE>
+static cudaError_t launch_prefill_p(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const PrefillParams& p, int max_rows, int sm, cudaStream_t stream) {
+  const bool padk = p.seqlens_k != nullptr && p.cu_q == nullptr;
+  return padk ? launch_prefill_d<D, ALIBI, ROPE, true>(tq, tk, tv, p, max_rows, sm, stream)
+              : launch_prefill_d<D, ALIBI, ROPE, false>(tq, tk, tv, p, max_rows, sm, stream);
 }
 
 template <int D>
 static cudaError_t launch_prefill_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                      const PrefillParams& p, int max_rows, int sm, cudaStream_t stream) {
   const bool alibi = p.alibi != nullptr, rope = p.rope_cos != nullptr;
-  if (alibi) return rope ? launch_prefill_d<D, true, true>(tq, tk, tv, p, max_rows, sm, stream)
-                         : launch_prefill_d<D, true, false>(tq, tk, tv, p, max_rows, sm, stream);
-  return rope ? launch_prefill_d<D, false, true>(tq, tk, tv, p, max_rows, sm, stream)
-              : launch_prefill_d<D, false, false>(tq, tk, tv, p, max_rows, sm, stream);
+  if (alibi) return rope ? launch_prefill_p<D, true, true>(tq, tk, tv, p, max_rows, sm, stream)
+                         : launch_prefill_p<D, true, false>(tq, tk, tv, p, max_rows, sm, stream);
+  return rope ? launch_prefill_p<D, false, true>(tq, tk, tv, p, max_rows, sm, stream)
+              : launch_prefill_p<D, false, false>(tq, tk, tv, p, max_rows, sm, stream);
 }
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -148,6 +148,31 @@ def test_zero_length_keys_give_zero_rows():
     assert torch.all(o == 0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_nan_in_padding_past_seqlens_k_is_ignored(d):
+    # padded layout: K/V rows past a sequence's valid length are in-bounds memory the caller may
+    # leave as anything (here NaN and Inf); they must not reach O or the LSE
+    import flashattention_forward_fa_gb300 as fa
+    case = PrefillCase("nan_padding", B=3, Hq=4, Hkv=2, Nq=200, Nk=300, d=d, layout="padded", causal=True,
+                       len_q=[200, 90, 1], len_k=[300, 131, 64], seed=330 + d)
+    x = make_prefill(case)
+    k, v = x.k.clone(), x.v.clone()
+    for b, lk in enumerate(x.len_k):
+        k[b, lk:] = float("nan")
+        v[b, lk:] = float("nan")
+        v[b, lk::3] = float("inf")
+    sq = torch.tensor(x.len_q, dtype=torch.int32, device="cuda")
+    sk = torch.tensor(x.len_k, dtype=torch.int32, device="cuda")
+    o, lse = fa.fa_fwd(x.q.cuda(), k.cuda(), v.cuda(), causal=True, seqlens_q=sq, seqlens_k=sk)
+    torch.cuda.synchronize()
+    rows = oracle.all_rows(x.len_q, case.Hq)
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    ro, rl = oracle_prefill_rows(x, rows)  # the oracle reads only the valid rows of the clean tensors
+    check(go, gl, ro, rl, case.name)
+    assert torch.isfinite(o.float()).all()
+    assert fa.fa_device_status() == 0
+
+
 # ------------------------------------------------------------------ invariances (GPU vs GPU)
 
 def test_varlen_packed_equals_per_sequence_dense():
