@@ -103,3 +103,31 @@ def test_decode_matches_prefill_last_row():
     po, pl = fa.fa_fwd(q4, x.k_cache.cuda(), x.v_cache.cuda(), causal=True)
     assert (po[:, 0].float() - o.float()).abs().max().item() <= 1e-2
     assert (pl[:, :, 0] - lse).abs().max().item() <= 1e-3
+
+
+def test_decode_replays_from_cuda_graph():
+    # a serving loop captures the decode once and replays it per token with new inputs in the same
+    # buffers: the captured launches must read the buffers at replay time and match eager calls
+    import flashattention_forward_fa_gb300 as fa
+    c = shrink(DECODE_CACHE, name="graph", B=8, Ncap=2048, len_range=(100, 2048), seed=71)
+    x = make_decode(c)
+    q, kc, vc = x.q.cuda(), x.k_cache.cuda(), x.v_cache.cuda()
+    lens = torch.tensor(x.lens, dtype=torch.int32, device="cuda")
+    S = fa.fa_decode_max_splits(c.B, c.Hq, c.Hkv, c.Ncap, 0, x.lens, 0)
+    ws = torch.empty((fa.decode_workspace_size(c.B, c.Hq, c.d, S) + 3) // 4, dtype=torch.float32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((c.B, c.Hq), dtype=torch.float32, device="cuda")
+    fa.fa_decode(q, kc, vc, lens, seqlens_k_host=x.lens, workspace=ws, out=o, lse=lse)  # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.fa_decode(q, kc, vc, lens, seqlens_k_host=x.lens, workspace=ws, out=o, lse=lse)
+    gen = torch.Generator("cpu").manual_seed(72)
+    for step in range(3):
+        q.copy_(torch.randn(q.shape, generator=gen).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        o_ref, lse_ref = fa.fa_decode(q, kc, vc, lens, seqlens_k_host=x.lens)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), f"replay {step} differs from an eager call"
+    assert fa.fa_device_status() == 0
