@@ -24,7 +24,8 @@ struct PrefillParams {
   const float* rope_cos;
   const float* rope_sin;
   int rope_rows, rope_dim;
-  int n_qblk;              // 256-row blocks per sequence (set by the launcher)
+  int n_qblk;              // row blocks per sequence (set by the launcher)
+  int pair_heads;          // items pair two query heads of one KV group (set by the launcher)
 };
 
 struct RopeParams {

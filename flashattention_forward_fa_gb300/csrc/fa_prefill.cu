@@ -11,7 +11,9 @@
 // How (GB300-first; the pages' Cube/Vector double buffer is only prior art):
 //   persistent: one CTA per SM walks its share of the work items (a snake over the
 //   CTAs of the heaviest-first item list); one item = two 128-row Q tiles (A, B) of
-//   one (sequence, query head).  The K/V rings and every barrier phase run on across
+//   one sequence that read the same K/V: consecutive row tiles of one query head, or,
+//   with an even number of query heads per KV head, the same rows of two heads of one
+//   group (identical K/V ranges and masks).  The K/V rings and every barrier phase run on across
 //   items, so the next item's Q load, K/V loads and first S overlap the current
 //   item's last P V and epilogue instead of a CTA launch, TMEM allocation and
 //   pipeline fill per item.  12 warps:
@@ -185,35 +187,51 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// One work item: two consecutive 128-row Q tiles of one (sequence, query head).
+// One work item: two 128-row Q tiles of one sequence that read the same K/V head.  Without
+// grouping (one query head per KV head) they are consecutive row tiles of one query head; with an
+// even number of query heads per KV head they are the same rows of two query heads of one group,
+// whose K/V ranges and masks are then identical (no step of the walk feeds only one tile).
 struct WorkItem {
-  int h, q0;
-  SeqInfo s;
+  int h, q0;       // tile A: query head, first row (tile B: item_head / item_row0)
+  SeqInfo s;       // lse_row0 for tile A's head
   QTileRange ra, rb;
-  int u0, u1;  // union of the two tiles' K/V tile ranges (contiguous: tile B's rows follow
-               // tile A's, so B's first visible key is at most one past A's last); empty if u0 >= u1
+  int u0, u1;  // union of the two tiles' K/V tile ranges (contiguous: tile B's rows equal or
+               // follow tile A's, so B's first visible key is at most one past A's last); empty if u0 >= u1
   bool live;   // the block holds output rows (q0 < rows_out)
 };
 
-// Item w: query head fastest, then sequence, then 256-row block; masked problems (causal or
-// window) take the blocks latest-first, which is heaviest-first for causal.
+// Item w: head (pair) fastest, then sequence, then row block; masked problems (causal or window)
+// take the blocks latest-first, which is heaviest-first for causal.
 template <int BM, int BN>
 __device__ __forceinline__ WorkItem work_item(const PrefillParams& p, int w) {
   WorkItem it;
-  it.h = w % p.Hq;
-  const int rest = w / p.Hq;
+  const bool hp = p.pair_heads != 0;
+  const int nh = hp ? p.Hq / 2 : p.Hq;
+  const int hh = w % nh;
+  const int rest = w / nh;
   const int b = rest % p.B;
   const int j = rest / p.B;
   const int qblk = (p.causal || p.window > 0) ? p.n_qblk - 1 - j : j;
-  it.q0 = qblk * (2 * BM);
+  it.h = hp ? 2 * hh : hh;
+  it.q0 = qblk * (hp ? BM : 2 * BM);
   it.s = seq_info(p, b, it.h);
-  it.live = it.q0 < it.s.rows_out;
+  it.live = it.q0 >= 0 && it.q0 < it.s.rows_out;  // never a block outside the rows
   it.ra = qtile_range<BM, BN>(it.s, it.q0, p.causal, p.window);
-  it.rb = qtile_range<BM, BN>(it.s, it.q0 + BM, p.causal, p.window);
+  it.rb = qtile_range<BM, BN>(it.s, hp ? it.q0 : it.q0 + BM, p.causal, p.window);
   const bool act_a = it.ra.t1 > it.ra.t0, act_b = it.rb.t1 > it.rb.t0;
   it.u0 = act_a ? (act_b ? min(it.ra.t0, it.rb.t0) : it.ra.t0) : (act_b ? it.rb.t0 : 0);
   it.u1 = act_a ? (act_b ? max(it.ra.t1, it.rb.t1) : it.ra.t1) : (act_b ? it.rb.t1 : 0);
   return it;
+}
+
+// Tile X's query head and first row (tile B: the next head of the pair, or the next row tile).
+template <int BM>
+__device__ __forceinline__ int item_head(const PrefillParams& p, const WorkItem& it, int X) {
+  return it.h + (X && p.pair_heads ? 1 : 0);
+}
+template <int BM>
+__device__ __forceinline__ int item_row0(const PrefillParams& p, const WorkItem& it, int X) {
+  return it.q0 + (X && !p.pair_heads ? BM : 0);
 }
 
 // The k-th item of this CTA: a snake over the resident CTAs (round k runs forward for even k,
@@ -287,9 +305,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using C = PrefillCfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = p.Hq * p.B * p.n_qblk;
+  const int n_items = (p.pair_heads ? p.Hq / 2 : p.Hq) * p.B * p.n_qblk;  // as the launcher counts them
   const int n_rounds = (int)(((long long)n_items + gridDim.x - 1) / gridDim.x);
   constexpr bool rev = ALIBI;  // walk each item's K/V tiles last to first
+  // register split after setmaxnreg; the RoPE variants' softmax needs a little more (it keeps a
+  // second item in flight for the look-ahead rotation)
+  constexpr int REGS_S = (ROPE && D == 128) ? 208 : C::REGS_SOFTMAX;
+  constexpr int REGS_P = (ROPE && D == 128) ? 80 : C::REGS_PRODUCER;
+  static_assert(2 * 128 * REGS_S + 128 * REGS_P <= C::THREADS * (65536 / C::THREADS / 8 * 8), "register split");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -346,7 +369,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   // barrier phases below are running counts that continue from one item to the next.
   if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
-    setmaxnreg_inc<C::REGS_SOFTMAX>();
+    setmaxnreg_inc<REGS_S>();
     const int X = warp >> 2;               // 0: tile A, 1: tile B
     const int rg = tid & 127;              // row within the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -372,9 +395,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (w < 0) continue;
       const WorkItem it = work_item<C::BM, C::BN>(p, w);
       if (!it.live) continue;
-      const SeqInfo s = it.s;
+      SeqInfo s = it.s;
+      if (X && p.pair_heads) s.lse_row0 += p.cu_q ? (long long)p.cu_q[p.B] : (long long)p.Nq;  // the next head
       const QTileRange r = X ? it.rb : it.ra;
-      const int h = it.h;
+      const int h = item_head<C::BM>(p, it, X);
       const int i = r.q0 + rg;
       if (it.u1 > it.u0) ++n_q;
       const uint32_t v_first = v_next;  // V ring index of this item's first tile
@@ -607,7 +631,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ Q + K producer
-    setmaxnreg_dec<C::REGS_PRODUCER>();
+    setmaxnreg_dec<REGS_P>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -629,8 +653,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         for (int X = 0; X < C::NQT; ++X)
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, bar_q, c * 64, it.h,
-                        it.s.q_row0 + it.q0 + X * C::BM);
+            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, bar_q, c * 64, item_head<C::BM>(p, it, X),
+                        it.s.q_row0 + item_row0<C::BM>(p, it, X));
         ++n_q;
         const int hkv = it.h / p.group;
         // Bring the next item's Q and first K tiles into L2 now: its Q load can only start once
@@ -645,7 +669,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           for (int X = 0; X < C::NQT; ++X)
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-              tma_prefetch_l2_3d(&tm_q, c * 64, nx.h, nx.s.q_row0 + nx.q0 + X * C::BM);
+              tma_prefetch_l2_3d(&tm_q, c * 64, item_head<C::BM>(p, nx, X), nx.s.q_row0 + item_row0<C::BM>(p, nx, X));
           for (int j = 0; j < C::KST && j < nx.u1 - nx.u0; ++j) {
             const int t2 = rev ? nx.u1 - 1 - j : nx.u0 + j;
 #pragma unroll
@@ -676,7 +700,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ V producer
-    setmaxnreg_dec<C::REGS_PRODUCER>();
+    setmaxnreg_dec<REGS_P>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
       uint32_t gv = 0;  // V tiles issued (ring index)
@@ -708,7 +732,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   } else if (warp == 10) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop converged; one elected lane issues each instruction.
-    setmaxnreg_dec<C::REGS_PRODUCER>();
+    setmaxnreg_dec<REGS_P>();
     const uint32_t leader = elect_one_sync() ? 1u : 0u;
     // Descriptors are built once; per MMA only the start-address field (bits 0..13, in 16-byte
     // units) moves, by an offset that is a compile-time constant after unrolling.
@@ -812,7 +836,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     mbar_wait_drain(mma_done, 0);
     __syncwarp();
   } else {
-    setmaxnreg_dec<C::REGS_PRODUCER>();  // warp 11: idle, its registers go to the softmax warps
+    setmaxnreg_dec<REGS_P>();  // warp 11: idle, its registers go to the softmax warps
   }
   tc_fence_before();
   __syncthreads();
@@ -841,9 +865,11 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   // lengths, so that the static order balances; with per-sequence lengths the item costs are
   // unknown here, and one CTA per item lets the hardware scheduler balance them.
   PrefillParams q = p;
-  const int rows_per_item = C::NQT * C::BM;
+  // an even number of query heads per KV head: pair heads (same rows, same K/V), else row tiles
+  q.pair_heads = (p.group % 2 == 0) ? 1 : 0;
+  const int rows_per_item = q.pair_heads ? C::BM : C::NQT * C::BM;
   q.n_qblk = (max_rows + rows_per_item - 1) / rows_per_item;
-  const long long n_items = (long long)q.Hq * q.B * q.n_qblk;
+  const long long n_items = (long long)(q.pair_heads ? q.Hq / 2 : q.Hq) * q.B * q.n_qblk;
   if (n_items <= 0) return cudaSuccess;
   if (n_items >= (1LL << 31)) return cudaErrorInvalidConfiguration;
   const bool uniform = !p.cu_q && !p.seqlens_q && !p.seqlens_k;
