@@ -507,3 +507,22 @@ def test_rope_scores_depend_only_on_relative_position():
     r_adj = orope.rotate(x, [1], c, s, 16)
     half = np.concatenate([x[..., 0::2], x[..., 1::2]], axis=-1)
     assert not np.allclose(r_adj, orope.rotate(half, [1], c, s, 16))
+
+
+# ------------------------------------------------------------------ stored oracle outputs (regression)
+
+def test_oracle_matches_its_stored_outputs():
+    # tests/golden/oracle_small.json was written by tests/golden/make_golden.py from the oracle; a
+    # change to the oracle's arithmetic shows up here (and must name the passage that justifies it)
+    import json
+    import os
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    sys.path.insert(0, os.path.join(here, "golden"))
+    import make_golden
+    stored = json.load(open(os.path.join(here, "golden", "oracle_small.json")))["cases"]
+    fresh = make_golden.build()
+    assert [c["name"] for c in stored] == [c["name"] for c in fresh]
+    for a, b in zip(stored, fresh):
+        np.testing.assert_allclose(b["o"], a["o"], rtol=0, atol=1e-12, err_msg=a["name"])
+        np.testing.assert_allclose(b["lse"], a["lse"], rtol=0, atol=1e-12, err_msg=a["name"])
