@@ -246,9 +246,13 @@ def oracle_sample_rate(target_s: float, seed: int = 0):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+LAST_STATS: dict = {}  # per-fn median / min of the last time_steps call
+
+
 def time_steps(fns, steps: int, stream):
     """Run ``steps`` steps; each step calls every fn in order.  Events around each fn on the
-    launching stream.  Returns (per-fn mean ms, total region ms)."""
+    launching stream.  Returns (per-fn mean ms, total region ms); per-fn median and min are left
+    in LAST_STATS."""
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
     torch.cuda.synchronize()
     for s in range(steps):
@@ -257,7 +261,10 @@ def time_steps(fns, steps: int, stream):
             fn()
             evs[s][i + 1].record(stream)
     torch.cuda.synchronize()
-    per = [sum(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)) / steps for i in range(len(fns))]
+    times = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)] for i in range(len(fns))]
+    per = [sum(t) / steps for t in times]
+    LAST_STATS["median"] = [statistics.median(t) for t in times]
+    LAST_STATS["min"] = [min(t) for t in times]
     total = evs[0][0].elapsed_time(evs[-1][-1])
     return per, total
 
@@ -344,6 +351,7 @@ def gpu_arm(args, world, rank, local):
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         (pre_ms, dec_ms), total_ms = time_steps([prefill, decode], args.steps, stream)
+        (pre_med, dec_med), (pre_min, dec_min) = LAST_STATS["median"], LAST_STATS["min"]
     barrier(world)
     pre_ms_max = max_over_ranks(pre_ms, world)
     dec_ms_max = max_over_ranks(dec_ms, world)
@@ -419,6 +427,10 @@ def gpu_arm(args, world, rank, local):
             "decode_bytes_per_step": dbytes,
             "prefill_ms": round(pre_ms_max, 4),
             "decode_ms": round(dec_ms_max, 4),
+            "prefill_ms_median": round(pre_med, 4),
+            "prefill_ms_min": round(pre_min, 4),
+            "decode_ms_median": round(dec_med, 4),
+            "decode_ms_min": round(dec_min, 4),
         },
         "roofline": {"bound": "tensor", "achieved": round(ach_pre, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(ach_pre / peaks["bf16_tflops"], 4),
