@@ -311,7 +311,7 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int B, int Hkv, int group, int Ncap, int window, const int* lens_host, int num_splits,
-                       int sm_count, int nq = 1) {
+                       int sm_count) {
   const int bn = fa::decode_block_n();
   const int cap = window > 0 ? (window < Ncap ? window : Ncap) : Ncap;
   long long total = 0;
@@ -329,11 +329,11 @@ DecodePlan plan_decode(int B, int Hkv, int group, int Ncap, int window, const in
   if (num_splits > 0) {
     chunk = (longest + num_splits - 1) / num_splits;
   } else {
-    // Aim for ~8 resident-CTA waves of equal-sized chunks so the tail wave is short.  With several
-    // new tokens per sequence every chunk writes (and the combine reads) nq times the partials, so
-    // take ~4 waves of larger chunks: fewer splits halve that traffic (and never need more
-    // workspace than the single-token plan fa_decode_max_splits reports).
-    const long long units = (long long)sm_count * 2 * (nq > 1 ? 4 : 8);
+    // Aim for ~4 resident-CTA waves of equal-sized chunks: enough that the tail wave is short,
+    // few enough that the split partials (written here, read back by the combine; nq times more
+    // with several new tokens) stay a small share of the bytes.  Measured on decode_cache:
+    // 2, 3, 4, 6 and 8 waves took 181.8, 179.6, 178.5, 179.6 and 180.6 us.
+    const long long units = (long long)sm_count * 2 * 4;
     const long long row_blocks = (long long)Hkv * ((group + 15) / 16);
     const long long keys = total * row_blocks;
     chunk = (int)((keys + units - 1) / units);
@@ -400,7 +400,7 @@ fa_status fa_decode_ex(const fa_decode_args* a, fa_stream_t stream) {
   // boundary at or below the window start: plan with 63 more
   const int plan_window = window > 0 ? window + (nq - 1) + (paged ? 63 : 0) : window;
   const DecodePlan pl =
-      plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, a->seqlens_k_host, a->num_splits, di->sm_count, nq);
+      plan_decode(B, Hkv, Hq / Hkv, cap, plan_window, a->seqlens_k_host, a->num_splits, di->sm_count);
   const size_t need = fa_decode_workspace_size(B * nq, Hq, d, pl.max_splits);
   if (!a->workspace) return fail(FA_ERR_INVALID, "workspace must be non-null (%zu bytes needed)", need);
   if (!aligned16(a->workspace)) return fail(FA_ERR_INVALID, "workspace must be 16-byte aligned");
