@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const float slope2 = ALIBI ? p.alibi[h] * 1.4426950408889634f : 0.f;  // m_h in log2 units
       float m = -INFINITY;  // running max used for exponentiation (log2 units)
       float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
-      float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
+      float lr = 0.f;       // ALiBi: running sum of the same weights rounded to bf16 (normalises O)
       if (ROPE && rot_k != k) ok = rotate_q(it, n_q - 1);
       for (int t = rev ? r.t1 - 1 : r.t0; ok && (rev ? t >= r.t0 : t < r.t1); t += rev ? -1 : 1, ++n_sx) {
         const int n = rev ? r.t1 - 1 - t : t - r.t0;  // position of tile t in the walk
@@ -537,14 +537,17 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
         if (need) {
           l *= alpha;
-          lr *= alpha;
+          if (ALIBI) lr *= alpha;
           m = m_new;
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        // P V runs on bf16-rounded weights; normalising O by the sum of those same rounded
-        // weights keeps O an exact convex combination of V rows, while the LSE uses the fp32 sum.
-        // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift, and both sums
-        // (two accumulators each to keep the dependency chains short).
+        // P V runs on bf16-rounded weights.  Without ALiBi the base m is the row's true max, whose
+        // weight is exactly 1, and O is normalised by the fp32 sum, as the LSE is.  With ALiBi the
+        // base may lie above the true max (the per-chunk bound), so even the largest weight is
+        // rounded: O is then normalised by the sum of the rounded weights, which keeps it an
+        // exact convex combination of V rows (a row that sees one key returns that V row).
+        // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift and the sums (two
+        // accumulators each to keep the dependency chains short).
         const uint64_t sl2x2 = f2_pack(xs_t, xs_t), negm2 = f2_pack(-m_use, -m_use);
         // ALiBi: exponent addend b_j - m per key pair, eight chains stepping 16 keys
         uint64_t bm[8];
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
             ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
             pk[j] = pack_bf16x2(e0, e1);
-            bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
+            if (ALIBI) bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
           }
           tmem_st16(t_lane + colS + 16 * c, pk);
         }
@@ -576,7 +579,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           float a0, a1;
           f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
           l += a0 + a1;
-          lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+          if (ALIBI) lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -608,7 +611,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (ok) {
         tc_fence_after();
         const bool store = i < s.Lq;
-        const float inv = lr > 0.f ? 1.0f / lr : 0.f;
+        const float nrm = ALIBI ? lr : l;
+        const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(s.q_row0 + i) * p.Hq + h) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
