@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   constexpr bool rev = ALIBI;  // walk each item's K/V tiles last to first
   // register split after setmaxnreg; the RoPE variants' softmax needs a little more (it keeps a
   // second item in flight for the look-ahead rotation)
-  constexpr int REGS_S = (ROPE && D == 128) ? 208 : C::REGS_SOFTMAX;
-  constexpr int REGS_P = (ROPE && D == 128) ? 80 : C::REGS_PRODUCER;
+  constexpr int REGS_S = (ROPE && D == 128) ? 216 : C::REGS_SOFTMAX;
+  constexpr int REGS_P = (ROPE && D == 128) ? 72 : C::REGS_PRODUCER;
   static_assert(2 * 128 * REGS_S + 128 * REGS_P <= C::THREADS * (65536 / C::THREADS / 8 * 8), "register split");
 
   extern __shared__ uint8_t smem_raw[];
@@ -801,32 +801,28 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const int tn = rev ? t - 1 : t + 1;             // the next tile of the walk
         const uint32_t gki = gk + (uint32_t)j, gvi = gv + (uint32_t)j;
         const bool nxt = rev ? tn >= it.u0 : tn < it.u1;
-        bool v_ready = false, k_ready = false;
+        // This step's operands first: V(t) for its P V and K(t+1) for the next S.  They have
+        // normally landed long before; waiting for them here, while the softmax still works on
+        // P(t), keeps both waits off the path from P(t) to the tensor core.
+        const bool pv_a = t >= it.ra.t0 && t < it.ra.t1, pv_b = t >= it.rb.t0 && t < it.rb.t1;
+        const bool s_a = nxt && tn >= it.ra.t0 && tn < it.ra.t1, s_b = nxt && tn >= it.rb.t0 && tn < it.rb.t1;
+        if (pv_a || pv_b)
+          ok = __all_sync(0xffffffffu, mbar_wait(&v_full[gvi % C::VST], (gvi / C::VST) & 1, abort_flag, p.err));
+        if (ok && (s_a || s_b))
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&k_full[(gki + 1) % C::KST], ((gki + 1) / C::KST) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int X = 0; X < C::NQT; ++X) {
-          const QTileRange& r = X ? it.rb : it.ra;
-          if (t >= r.t0 && t < r.t1) {
+          if (X ? pv_b : pv_a) {
             ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], n_p[X] & 1, abort_flag, p.err));
             ++n_p[X];
-            if (ok && !v_ready) {
-              ok = __all_sync(0xffffffffu,
-                              mbar_wait(&v_full[gvi % C::VST], (gvi / C::VST) & 1, abort_flag, p.err));
-              v_ready = true;
-            }
             if (!ok) break;
             tc_fence_after();
-            issue_pv(X, t, gvi, r);
+            issue_pv(X, t, gvi, X ? it.rb : it.ra);
           }
-          if (nxt && tn >= r.t0 && tn < r.t1) {
-            if (!k_ready) {
-              ok = __all_sync(0xffffffffu, mbar_wait(&k_full[(gki + 1) % C::KST], ((gki + 1) / C::KST) & 1,
-                                                     abort_flag, p.err));
-              if (!ok) break;
-              k_ready = true;
-              tc_fence_after();
-            }
-            issue_s(X, gki + 1);
-          }
+          if (X ? s_b : s_a) issue_s(X, gki + 1);
         }
         if (!ok) break;
         umma_commit_by(leader, &v_empty[gvi % C::VST]);

@@ -173,6 +173,41 @@ def test_nan_in_padding_past_seqlens_k_is_ignored(d):
     assert fa.fa_device_status() == 0
 
 
+@pytest.mark.parametrize("d,causal,window", [(128, True, 0), (64, True, 0), (128, False, 0), (64, True, 200)],
+                         ids=["d128_causal", "d64_causal", "d128_noncausal", "d64_window200"])
+def test_rising_scores_move_the_base_on_every_tile(d, causal, window):
+    # Scores that rise along the keys by ~12 log2 units per 128-key tile: every tile's max exceeds
+    # the running max by more than 2^8, so on every tile after a walk's first the exponent base
+    # moves, O is rescaled and the tile's weights are recomputed (on diagonal and window tiles from
+    # re-masked scores).  Neighbouring keys differ by ~0.065 in the exponent, so each row still
+    # spreads its weight over a few dozen keys.
+    import math
+    case = PrefillCase(f"rising_d{d}", B=1, Hq=4, Hkv=2, Nq=640, Nk=700, d=d, causal=causal, window=window,
+                       seed=340 + d)
+    x = make_prefill(case)
+    g = torch.Generator().manual_seed(341)
+    u = torch.randn(d, generator=g)
+    u = u / u.norm()
+    a = 4.0                                              # query component along u
+    beta = 0.065 / (case.softmax_scale * a)             # key component per position: 0.065 nat per key
+    ramp = torch.arange(case.Nk, dtype=torch.float32) * beta
+    x.q = (x.q.float() + a * u).to(torch.bfloat16)
+    x.k = (x.k.float() * 0.25 + ramp[None, :, None, None] * u).to(torch.bfloat16)
+    o, lse, _ = _parity_of(x)
+    assert torch.isfinite(o.float()).all()
+
+
+def _parity_of(x):
+    import flashattention_forward_fa_gb300 as fa
+    o, lse = gpu_prefill(x)
+    rows = oracle.all_rows(x.len_q, x.case.Hq)
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    ro, rl = oracle_prefill_rows(x, rows)
+    res = check(go, gl, ro, rl, x.case.name, strict=False)  # |O| ~ |V| > 1.28: the sharpened-score bound
+    assert fa.fa_device_status() == 0
+    return o, lse, res
+
+
 # ------------------------------------------------------------------ invariances (GPU vs GPU)
 
 def test_varlen_packed_equals_per_sequence_dense():
