@@ -214,8 +214,9 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
   if ((st = device_info(&di)) != FA_OK) return st;
   if ((st = get_encoder()) != FA_OK) return st;
   const int bm = fa::prefill_box_rows();
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((st = make_map(&tq, a->q, d, Hq, q_rows, bm, "q")) != FA_OK) return st;
+  if ((st = make_map(&to, a->o, d, Hq, q_rows, bm, "o")) != FA_OK) return st;
   if ((st = make_map(&tk, a->k, d, Hkv, k_rows, 128, "k")) != FA_OK) return st;
   if ((st = make_map(&tv, a->v, d, Hkv, k_rows, 128, "v")) != FA_OK) return st;
   fa::PrefillParams p{};
@@ -242,7 +243,7 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
     p.rope_rows = a->rope_rows;
     p.rope_dim = a->rope_dim;
   }
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, max_rows, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, max_rows, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }

@@ -63,8 +63,9 @@ struct DecodeParams {
 
 // max_rows: rows per sequence (padded layout) or the longest sequence (packed layout).
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& to,
                            const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream);
-int prefill_box_rows();  // rows of one TMA box of Q / K / V
+int prefill_box_rows();  // rows of one TMA box of Q / K / V / O
 
 cudaError_t launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           cudaStream_t stream);  // paged when p.page_size > 0

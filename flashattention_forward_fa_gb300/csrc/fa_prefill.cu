@@ -68,10 +68,13 @@ struct PrefillCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
+  // O staging, one buffer per tile: a 64-column box of its 128 rows in the layout TMA stores from
+  static constexpr int OFF_OST = OFF_V + VST * KV_BYTES;
+  static constexpr int O_BOX = BM * 64 * 2;
+  static constexpr int OFF_BAR = OFF_OST + NQT * O_BOX;
   // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2], q_empty
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2 + 1;
+  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2], q_empty, o_free[2], o_staged[2]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2 + 1 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
@@ -302,7 +305,8 @@ __device__ __forceinline__ bool rotate_q_tile(const PrefillParams& p, const Work
 template <int D, bool ALIBI, bool ROPE, bool PADK>
 __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const PrefillParams p) {
   using C = PrefillCfg<D>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = (p.pair_heads ? p.Hq / 2 : p.Hq) * p.B * p.n_qblk;  // as the launcher counts them
@@ -331,6 +335,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint64_t* mma_done = o_final + 2;
   uint64_t* q_ready = mma_done + 1;     // [2]: four warp arrivals once Q_X is rotated (RoPE only)
   uint64_t* q_empty = q_ready + 2;      // every S of an item has run: Q may be overwritten
+  uint64_t* o_free = q_empty + 1;       // [2]: tile X's last O store has read its staging buffer
+  uint64_t* o_staged = o_free + 2;      // [2]: four warp arrivals once a box of tile X's O rows is staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
 
@@ -354,6 +360,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     mbar_init(&q_ready[0], 4);
     mbar_init(&q_ready[1], 4);
     mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_free[i], 1);
+      mbar_init(&o_staged[i], 4);
+    }
     fence_barrier_init();
   }
   if (warp == 10) {
@@ -382,6 +392,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
     uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
     uint32_t v_next = 0;  // V ring index of the next item's first tile
+    uint32_t n_box = 0;   // O boxes of this tile staged and stored so far (o_staged / o_free phase)
     int rot_k = -1;     // RoPE: the round whose item already has this tile's Q rotated
     bool ok = true;
     // RoPE rotation of Q_X (rotate_q_tile).  bar_q phases are waited strictly in order (a parity
@@ -405,7 +416,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (it.u1 > it.u0) v_next += (uint32_t)(it.u1 - it.u0);
       if (r.t1 <= r.t0) {  // this tile's rows see no key: O = 0, LSE = -inf (and zero padding rows)
         if (ROPE && it.u1 > it.u0) ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
-        if (i < s.rows_out) store_row_zero<D>(p, s, h, i);
+        if (ok && i < s.rows_out) store_row_zero<D>(p, s, h, i);
         continue;
       }
       const int pos = i + s.Lk - s.Lq;
@@ -613,26 +624,82 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         const bool store = i < s.Lq;
         const float nrm = ALIBI ? lr : l;
         const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(s.q_row0 + i) * p.Hq + h) * D;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(t_lane + colO + c, ov);
-          tmem_ld_wait(ov);
-          if (store) {
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              w[j] = pack_bf16x2(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
-        }
         if (store && p.lse) p.lse[s.lse_row0 + i] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        if (!store && i < s.rows_out) store_row_zero<D>(p, s, h, i);
+        // 64 columns of this row of O_X (box bx), normalised and packed to bf16 pairs
+        auto load_box = [&](int bx, uint32_t (&ow)[32]) {
+          uint32_t ov0[32], ov1[32];
+          tmem_ld32(t_lane + colO + 64 * bx, ov0);
+          tmem_ld32(t_lane + colO + 64 * bx + 32, ov1);
+          tmem_ld_wait(ov0);
+          tmem_ld_wait(ov1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            ow[j] = pack_bf16x2(__uint_as_float(ov0[2 * j]) * inv, __uint_as_float(ov0[2 * j + 1]) * inv);
+            ow[16 + j] = pack_bf16x2(__uint_as_float(ov1[2 * j]) * inv, __uint_as_float(ov1[2 * j + 1]) * inv);
+          }
+        };
+        if (r.q0 + C::BM <= s.Lq) {
+          // Every row of the tile lies inside the sequence: stage its O in shared memory, one
+          // 64-column box at a time, in the 128-byte swizzled layout of the O tensor map, and write
+          // each box with one TMA store (whole lines, instead of one 16-byte piece of 32 rows per
+          // store instruction).  The buffer is this tile's own; a box may be staged once the
+          // previous box's store has read it (o_free; the wait for the last box of an epilogue is
+          // left to the next one).
+          uint8_t* stg = sm + C::OFF_OST + X * C::O_BOX;
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx) {
+            uint32_t ow[32];
+            load_box(bx, ow);
+            if (n_box > 0) {
+              if (bx == 0 && rg == 0) {
+                bulk_wait_read();
+                mbar_arrive(&o_free[X]);
+              }
+              ok = __all_sync(0xffffffffu, mbar_wait(&o_free[X], (n_box - 1) & 1, abort_flag, p.err));
+            }
+            if (ok) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4*>(stg + rg * 128 + ((q ^ (rg & 7)) << 4)) =
+                    make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+              fence_async_smem();  // the TMA store reads the staged rows through the async proxy
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&o_staged[X]);
+              if (rg == 0) {
+                ok = mbar_wait(&o_staged[X], n_box & 1, abort_flag, p.err);  // all four warps' rows
+                if (ok) {
+                  tma_store_3d(&tm_o, stg, bx * 64, h, s.q_row0 + r.q0);
+                  bulk_commit();
+                  if (bx + 1 < D / 64) {
+                    bulk_wait_read();
+                    mbar_arrive(&o_free[X]);
+                  }
+                }
+              }
+              ok = __all_sync(0xffffffffu, ok);
+            }
+            ++n_box;
+            if (!ok) break;
+          }
+        } else {
+          // A ragged tile stores row by row: its rows past the sequence belong to the next
+          // sequence or are padding.
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(s.q_row0 + i) * p.Hq + h) * D;
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx) {
+            uint32_t ow[32];
+            load_box(bx, ow);  // TMEM loads are warp-wide: every lane takes part, stored or not
+            if (store) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                reinterpret_cast<uint4*>(orow)[8 * bx + q] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+            }
+          }
+          if (!store && i < s.rows_out) store_row_zero<D>(p, s, h, i);
+        }
       }
     }
+    if (rg == 0) bulk_wait_all();  // this thread's O stores are complete before the CTA exits
   } else if (warp == 8) {
     // ------------------------------------------------------------ Q + K producer
     setmaxnreg_dec<REGS_P>();
@@ -847,7 +914,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 }
 
 template <int D, bool ALIBI, bool ROPE, bool PADK>
-static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                                     const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
   using C = PrefillCfg<D>;
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
@@ -874,32 +941,32 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
   if (n_items >= (1LL << 31)) return cudaErrorInvalidConfiguration;
   const bool uniform = !p.cu_q && !p.seqlens_q && !p.seqlens_k;
   const unsigned grid = (unsigned)(uniform && n_items > sm_count ? sm_count : n_items);
-  fa_prefill_kernel<D, ALIBI, ROPE, PADK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, q);
+  fa_prefill_kernel<D, ALIBI, ROPE, PADK><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }
 
 template <int D, bool ALIBI, bool ROPE>
-static cudaError_t launch_prefill_p(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t launch_prefill_p(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                                     const PrefillParams& p, int max_rows, int sm, cudaStream_t stream) {
   const bool padk = p.seqlens_k != nullptr && p.cu_q == nullptr;
-  return padk ? launch_prefill_d<D, ALIBI, ROPE, true>(tq, tk, tv, p, max_rows, sm, stream)
-              : launch_prefill_d<D, ALIBI, ROPE, false>(tq, tk, tv, p, max_rows, sm, stream);
+  return padk ? launch_prefill_d<D, ALIBI, ROPE, true>(tq, tk, tv, to, p, max_rows, sm, stream)
+              : launch_prefill_d<D, ALIBI, ROPE, false>(tq, tk, tv, to, p, max_rows, sm, stream);
 }
 
 template <int D>
-static cudaError_t launch_prefill_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t launch_prefill_dd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                                      const PrefillParams& p, int max_rows, int sm, cudaStream_t stream) {
   const bool alibi = p.alibi != nullptr, rope = p.rope_cos != nullptr;
-  if (alibi) return rope ? launch_prefill_p<D, true, true>(tq, tk, tv, p, max_rows, sm, stream)
-                         : launch_prefill_p<D, true, false>(tq, tk, tv, p, max_rows, sm, stream);
-  return rope ? launch_prefill_p<D, false, true>(tq, tk, tv, p, max_rows, sm, stream)
-              : launch_prefill_p<D, false, false>(tq, tk, tv, p, max_rows, sm, stream);
+  if (alibi) return rope ? launch_prefill_p<D, true, true>(tq, tk, tv, to, p, max_rows, sm, stream)
+                         : launch_prefill_p<D, true, false>(tq, tk, tv, to, p, max_rows, sm, stream);
+  return rope ? launch_prefill_p<D, false, true>(tq, tk, tv, to, p, max_rows, sm, stream)
+              : launch_prefill_p<D, false, false>(tq, tk, tv, to, p, max_rows, sm, stream);
 }
 
-cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                            const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
-  return d == 64 ? launch_prefill_dd<64>(tq, tk, tv, p, max_rows, sm_count, stream)
-                 : launch_prefill_dd<128>(tq, tk, tv, p, max_rows, sm_count, stream);
+  return d == 64 ? launch_prefill_dd<64>(tq, tk, tv, to, p, max_rows, sm_count, stream)
+                 : launch_prefill_dd<128>(tq, tk, tv, to, p, max_rows, sm_count, stream);
 }
 
 int prefill_box_rows() { return PrefillCfg<128>::BM; }
