@@ -33,18 +33,24 @@
 //   means O_X already holds PV_X(t): the softmax may rescale O_X without a wait.
 //   The rescale is lazy: the exponent base only moves when a tile's max exceeds
 //   it by more than 2^8; the final O / l uses the same base, so it is exact.
+//   Per step the issuer waits for the step's V and next K first, then for each P in
+//   turn, so no wait sits between a P and its P V.  The epilogue stages a tile's O
+//   in shared memory (64 columns at a time, in the TMA layout) and writes it with
+//   TMA stores; a ragged tile stores row by row.
 //   With ALiBi (jsqmd page, §三 "ALiBi位置编码的线性偏置") each score gets
 //   -m_h |p - j| (p the query's absolute position) right after masking, folded into
 //   the same fused multiply-add that applies the softmax scale.
-//   With RoPE (jsqmd page, §三 "融合位置编码的Attention计算") each softmax thread rotates its
-//   own Q row in shared memory right after the TMA load, before the first S_X; K arrives
-//   rotated (a K tile is read by every CTA of its head, so it is rotated once, not per CTA).
+//   With RoPE (jsqmd page, §三 "融合位置编码的Attention计算") the softmax warps rotate
+//   the next item's Q tile in shared memory as soon as it lands (rotate_q_tile), before
+//   its first S_X; K arrives rotated (a K tile is read by every CTA of its head, so it is
+//   rotated once, not per CTA).
 //   Each Q tile visits only the K/V tiles its rows can see (causal / window
 //   tiles that are fully masked are never loaded or multiplied).  With ALiBi
 //   the walk starts at the last tile: the diagonal, where ALiBi scores peak,
 //   sets the running max early, so later tiles rarely move it and O is rarely
 //   rescaled; otherwise it starts at the first, so the CTAs of one head stream
-//   the same early K/V tiles at about the same time and share them in L2.  Only tiles crossing a mask edge or the ragged tail evaluate the mask.
+//   the same early K/V tiles at about the same time and share them in L2.  Only
+//   tiles crossing a mask edge or the ragged tail evaluate the mask.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
