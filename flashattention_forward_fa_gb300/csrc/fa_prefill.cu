@@ -90,9 +90,10 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 0, 1);   // P K-major (TMEM), V MN-major
   // Registers per thread after the split (setmaxnreg): the softmax warpgroups grow, the
-  // producer warpgroup shrinks.  Chosen so that neither side spills for either head dim.
-  static constexpr int REGS_SOFTMAX = (D == 128) ? 200 : 208;
-  static constexpr int REGS_PRODUCER = (D == 128) ? 96 : 72;
+  // producer warpgroup shrinks.  Chosen so that neither side spills for either head dim (at
+  // d=128, 216/72 measured 0.7 % faster than 200/96 without options, 1.7 % with ALiBi).
+  static constexpr int REGS_SOFTMAX = (D == 128) ? 216 : 208;
+  static constexpr int REGS_PRODUCER = 72;
   static_assert(2 * 128 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= THREADS * (65536 / THREADS / 8 * 8),
                 "register split exceeds the launch allocation");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -318,10 +319,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   const int n_items = (p.pair_heads ? p.Hq / 2 : p.Hq) * p.B * p.n_qblk;  // as the launcher counts them
   const int n_rounds = (int)(((long long)n_items + gridDim.x - 1) / gridDim.x);
   constexpr bool rev = ALIBI;  // walk each item's K/V tiles last to first
-  // register split after setmaxnreg; the RoPE variants' softmax needs a little more (it keeps a
-  // second item in flight for the look-ahead rotation)
-  constexpr int REGS_S = (ROPE && D == 128) ? 216 : C::REGS_SOFTMAX;
-  constexpr int REGS_P = (ROPE && D == 128) ? 72 : C::REGS_PRODUCER;
+  constexpr int REGS_S = C::REGS_SOFTMAX, REGS_P = C::REGS_PRODUCER;  // register split after setmaxnreg
   static_assert(2 * 128 * REGS_S + 128 * REGS_P <= C::THREADS * (65536 / C::THREADS / 8 * 8), "register split");
 
   extern __shared__ uint8_t smem_raw[];
