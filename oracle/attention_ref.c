@@ -18,8 +18,8 @@
  * Readings where the pages are silent (each listed in the design notes):
  *  - causal alignment is bottom-right: query row i of a sequence with Lq
  *    queries and Lk keys sits at absolute position p = i + Lk - Lq and may see
- *    key j iff j <= p (the jsqmd page, §二 "因果掩码与解码优化", only says "attend
- *    to earlier positions");
+ *    key j iff j <= p (the jsqmd page, §二 "因果掩码与解码优化", says only that a
+ *    position sees the ones before it);
  *  - sliding window w > 0: with causal, keys p - w < j <= p (the window holds
  *    the diagonal, so w = 1 keeps only key p); without causal, |p - j| < w;
  *    w <= 0 means no window (the jsqmd page, §一 "核心能力矩阵", names the mode only);

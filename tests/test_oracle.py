@@ -509,6 +509,91 @@ def test_rope_scores_depend_only_on_relative_position():
     assert not np.allclose(r_adj, orope.rotate(half, [1], c, s, 16))
 
 
+def _bf16_bits_of(v):
+    """The bf16 pattern of a float64 value that is exactly a bf16 number (its float32 upper half)."""
+    w = np.array([v], dtype=np.float32).view(np.uint32)[0]
+    assert (w & 0xFFFF) == 0, "not a bf16 value"
+    return int(w >> 16)
+
+
+def test_bf16_rounding_ties_neighbours_zeros():
+    # Worked from the format: near 1.0 the bf16 spacing is 2^-7 (1.0 = 0x3F80, next 0x3F81 = 1 + 2^-7).
+    r = orope.bf16_round_bits
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + 2.0 ** -8, 0x3F80),                  # a tie between 0x3F80 and 0x3F81: the even pattern
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),              # a tie between 0x3F81 and 0x3F82: the even pattern
+        (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),     # just above a tie: up
+        (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80),     # just below a tie: down
+        # above a tie by less than half a float32 ulp: rounding through float32 would first land on
+        # the tie and then go down to 0x3F80; one rounding of the float64 value goes up
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),
+        (-(1.0 + 2.0 ** -8), 0xBF80),
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001),                      # smallest subnormal
+        (2.0 ** -134, 0x0000),                      # half of it: a tie with zero, which is even
+        (3 * 2.0 ** -135, 0x0001),                  # above that tie
+        (3 * 2.0 ** -134, 0x0002),                  # a tie between 0x0001 and 0x0002: even
+        (2.0 ** -126 - 2.0 ** -140, 0x0080),        # rounds up onto the smallest normal
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),     # largest finite
+        ((2 - 2.0 ** -8) * 2.0 ** 127 - 2.0 ** 100, 0x7F7F),
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),     # the midpoint to 2^128 is a tie: even = infinity
+        (-3.0e39, 0xFF80),
+        (math.pi, 0x4049),                          # 3.140625 = 0x4049 is nearest to pi
+    ]
+    got = r(np.array([c[0] for c in cases]))
+    for (x, want), g in zip(cases, got):
+        assert int(g) == want, f"{x!r}: 0x{int(g):04X} != 0x{want:04X}"
+    nan = int(orope.bf16_round_bits(np.nan))
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x007F) != 0      # NaN stays NaN
+
+
+def test_bf16_rounding_is_the_nearest_bf16_value():
+    # Brute force over the format: list every finite non-negative bf16 value in order and pick, for
+    # each sample, the nearer of its two neighbours (on a tie, the one with the even pattern).
+    pats = np.arange(0x0000, 0x7F80, dtype=np.uint32)
+    vals = (pats << np.uint32(16)).view(np.float32).astype(np.float64)
+    assert np.all(np.diff(vals) > 0)
+    rng = np.random.default_rng(77)
+    mags = np.concatenate([
+        rng.standard_normal(20000) * 4,
+        np.exp(rng.uniform(-95, 88, 20000)),                        # the whole exponent range
+        vals[rng.integers(0, len(vals), 5000)],                     # exact bf16 values
+        0.5 * (vals[:-1] + vals[1:])[rng.integers(0, len(vals) - 1, 5000)],   # exact midpoints (ties)
+    ])
+    xs = np.concatenate([mags, -mags])
+    a = np.abs(xs)
+    hi = np.searchsorted(vals, a, side="left")          # vals[hi - 1] < a <= vals[hi]
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    exact = vals[hi] == a
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick_hi = exact | (dhi < dlo) | ((dhi == dlo) & (pats[hi] % 2 == 0))
+    want = np.where(pick_hi, pats[hi], pats[lo]).astype(np.uint32)
+    want = want | (np.signbit(xs).astype(np.uint32) << np.uint32(15))
+    got = orope.bf16_round_bits(xs).astype(np.uint32)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, e.g. {xs[bad[0]]!r}: 0x{got[bad[0]]:04X} vs 0x{want[bad[0]]:04X}"
+
+
+def test_rotate_bf16_rounds_the_fp64_rotation_once():
+    # rotate_bf16 = one RNE rounding of the fp64 rotation, element by element
+    x = torch.from_numpy(RNG.standard_normal((9, 2, 16)).astype(np.float32)).to(torch.bfloat16)
+    pos = [0, 1, 2, 3, 5, 8, 13, 21, 34]
+    c, s = orope.tables(40, 12)
+    exact = orope.rotate(x.to(torch.float64).numpy(), pos, c, s, 12)
+    got = orope.rotate_bf16(x, pos, c, s, 12)
+    assert got.dtype == torch.bfloat16
+    np.testing.assert_array_equal(got.view(torch.int16).numpy().view(np.uint16), orope.bf16_round_bits(exact))
+    # every rotated value is within half a bf16 spacing of the fp64 rotation
+    g = got.to(torch.float64).numpy()
+    _, e = np.frexp(np.abs(exact))
+    assert np.all(np.abs(g - exact) <= np.ldexp(1.0, np.maximum(e, -125) - 9))
+    np.testing.assert_array_equal(g[..., 12:], x.to(torch.float64).numpy()[..., 12:])
+
+
 # ------------------------------------------------------------------ stored oracle outputs (regression)
 
 def test_oracle_matches_its_stored_outputs():
