@@ -231,6 +231,8 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
   p.Hkv = Hkv;
   p.Nq = a->Nq;
   p.Nk = a->Nk;
+  p.total_q = packed ? a->total_q : 0;
+  p.total_k = packed ? a->total_k : 0;
   p.group = Hq / Hkv;
   p.scale_log2 = a->scale * kLog2e;
   p.causal = a->causal ? 1 : 0;

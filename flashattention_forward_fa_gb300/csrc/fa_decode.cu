@@ -404,7 +404,11 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     if (lse_out && lane == 0) *lse_out = -INFINITY;
     return;
   }
-  const int ns = min((nspan + p.chunk - 1) / p.chunk, p.max_splits);  // never read past the workspace
+  const int need = (nspan + p.chunk - 1) / p.chunk;  // chunks this sequence's keys fill
+  // A host length that understated the device length planned too few splits: the keys past
+  // max_splits chunks were not read.  Report it; never read past the workspace.
+  if (need > p.max_splits && lane == 0) atomicOr(p.err, kDevErrBounds);
+  const int ns = min(need, p.max_splits);
   const size_t prow0 = ((size_t)bt * p.Hq + hq) * p.max_splits;
   constexpr float LOG2E = 1.4426950408889634f;
   float mx = -INFINITY;

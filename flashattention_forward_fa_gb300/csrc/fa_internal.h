@@ -15,6 +15,7 @@ struct PrefillParams {
   const int* seqlens_q;    // padded layout: int32 [B] valid lengths (nullptr = full)
   const int* seqlens_k;
   int B, Hq, Hkv, Nq, Nk;  // dense/padded: rows per sequence; packed: max lengths
+  int total_q, total_k;     // packed: rows of q / k (the LSE is [Hq, total_q])
   int group;               // Hq / Hkv
   float scale_log2;        // scale * log2(e)
   int causal, window;

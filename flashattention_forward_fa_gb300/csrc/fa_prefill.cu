@@ -5,8 +5,8 @@
 // tiled evaluation of the jsqmd page "CANN Transformer算子库ops-transformer深度实践",
 // §二 "FlashAttention的融合计算思想" (Q split by rows, K/V by columns, every Q block
 // sweeps all K/V blocks on chip) with the max-subtracted fp32 softmax of the
-// hwcomputing.csdn.net page, §2.2 "数值稳定性优化" (its "two-stage max propagation"
-// realised as a running max whose changes rescale the accumulator).
+// hwcomputing.csdn.net page, §2.2 "数值稳定性优化" (the page carries the row maximum from one
+// block to the next; here that is a running max whose changes rescale the accumulator).
 //
 // How (GB300-first; the pages' Cube/Vector double buffer is only prior art):
 //   persistent: one CTA per SM walks its share of the work items (a snake over the
@@ -32,7 +32,8 @@
 //   Because S_X(t+1) is issued after PV_X(t), the completion of S_X(t+1) also
 //   means O_X already holds PV_X(t): the softmax may rescale O_X without a wait.
 //   The rescale is lazy: the exponent base only moves when a tile's max exceeds
-//   it by more than 2^8; the final O / l uses the same base, so it is exact.
+//   it by more than 8 log2 units (a factor 2^8); O and its normaliser share that base, so
+//   their ratio does not depend on it, and weights stay within (0, 2^8].
 //   Per step the issuer waits for the step's V and next K first, then for each P in
 //   turn, so no wait sits between a P and its P V.  The epilogue stages a tile's O
 //   in shared memory (64 columns at a time, in the TMA layout) and writes it with
@@ -107,13 +108,20 @@ struct SeqInfo {
 __device__ __forceinline__ SeqInfo seq_info(const PrefillParams& p, int b, int h) {
   SeqInfo s;
   if (p.cu_q) {
-    s.q_row0 = p.cu_q[b];
-    s.Lq = p.cu_q[b + 1] - s.q_row0;
-    s.k_row0 = p.cu_k[b];
-    s.Lk = p.cu_k[b + 1] - s.k_row0;
+    int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    // cu_seqlens that disagree with the totals and maxima the launch was sized for would send the
+    // plain stores (LSE, ragged rows) past the outputs: report it and skip the sequence.
+    if (!(0 <= q0 && q0 <= q1 && q1 <= p.total_q && q1 - q0 <= p.Nq && 0 <= k0 && k0 <= k1 &&
+          k1 <= p.total_k && k1 - k0 <= p.Nk)) {
+      atomicOr(p.err, kDevErrBounds);
+      q0 = q1 = k0 = k1 = 0;
+    }
+    s.q_row0 = q0;
+    s.Lq = q1 - q0;
+    s.k_row0 = k0;
+    s.Lk = k1 - k0;
     s.rows_out = s.Lq;
-    const int total_q = p.cu_q[p.B];
-    s.lse_row0 = (long long)h * total_q + s.q_row0;
+    s.lse_row0 = (long long)h * p.total_q + s.q_row0;
   } else {
     s.q_row0 = b * p.Nq;
     s.k_row0 = b * p.Nk;
@@ -411,7 +419,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const WorkItem it = work_item<C::BM, C::BN>(p, w);
       if (!it.live) continue;
       SeqInfo s = it.s;
-      if (X && p.pair_heads) s.lse_row0 += p.cu_q ? (long long)p.cu_q[p.B] : (long long)p.Nq;  // the next head
+      if (X && p.pair_heads) s.lse_row0 += p.cu_q ? (long long)p.total_q : (long long)p.Nq;  // the next head
       const QTileRange r = X ? it.rb : it.ra;
       const int h = item_head<C::BM>(p, it, X);
       const int i = r.q0 + rg;
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const float slope2 = ALIBI ? p.alibi[h] * 1.4426950408889634f : 0.f;  // m_h in log2 units
       float m = -INFINITY;  // running max used for exponentiation (log2 units)
       float l = 0.f;        // running sum of exp2(score*sl2 - m) in fp32 (gives the LSE)
-      float lr = 0.f;       // ALiBi: running sum of the same weights rounded to bf16 (normalises O)
+      float lr = 0.f;       // running sum of the same weights rounded to bf16 (normalises O)
       if (ROPE && rot_k != k) ok = rotate_q(it, n_q - 1);
       for (int t = rev ? r.t1 - 1 : r.t0; ok && (rev ? t >= r.t0 : t < r.t1); t += rev ? -1 : 1, ++n_sx) {
         const int n = rev ? r.t1 - 1 - t : t - r.t0;  // position of tile t in the walk
@@ -552,15 +560,19 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
         if (need) {
           l *= alpha;
-          if (ALIBI) lr *= alpha;
+          lr *= alpha;
           m = m_new;
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        // P V runs on bf16-rounded weights.  Without ALiBi the base m is the row's true max, whose
-        // weight is exactly 1, and O is normalised by the fp32 sum, as the LSE is.  With ALiBi the
-        // base may lie above the true max (the per-chunk bound), so even the largest weight is
-        // rounded: O is then normalised by the sum of the rounded weights, which keeps it an
-        // exact convex combination of V rows (a row that sees one key returns that V row).
+        // P V runs on bf16-rounded weights, so O is normalised by the sum of those same rounded
+        // weights (lr): O is then an exact convex combination of V rows, and a rounding error of a
+        // weight moves O only by its share times |v_j - O| (a row that sees one key returns that
+        // V row exactly).  Normalising by the unrounded sum instead measured up to 1.5e-2 off on
+        // rows dominated by two or three keys with |O| ~ 2.  The LSE uses the fp32 sum of the
+        // unrounded weights (l): from the rounded sum it would be up to 2.7e-3 off.  The base m may
+        // trail the row's max by up to 8 log2 units (the lazy rescale above), so weights reach
+        // 2^8; with ALiBi it may also lie above the true max (the per-chunk bound), which lowers
+        // every weight of the tile by a common factor.
         // Two lanes of fp32 per instruction (fma/add .f32x2): scale-and-shift and the sums (two
         // accumulators each to keep the dependency chains short).
         const uint64_t sl2x2 = f2_pack(xs_t, xs_t), negm2 = f2_pack(-m_use, -m_use);
@@ -573,10 +585,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             bm[u] = f2_pack(fmaf(ba, (float)(2 * u), bc) - m_use, fmaf(ba, (float)(2 * u + 1), bc) - m_use);
         }
         uint64_t ls[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-        float lr4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[C::BN / 32][16];  // the tile's P, bf16 pairs (kept for the rounded sum below)
 #pragma unroll
         for (int c = 0; c < C::BN / 32; ++c) {  // 32 scores -> 16 packed columns, stored at once
-          uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float x0, x1;
@@ -585,21 +596,30 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             if (ALIBI) bm[j & 7] = f2_add(bm[j & 7], bstep);
             const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
             ls[j & 1] = f2_add(ls[j & 1], f2_pack(e0, e1));
-            pk[j] = pack_bf16x2(e0, e1);
-            if (ALIBI) bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[j]);
+            pk[c][j] = pack_bf16x2(e0, e1);
           }
-          tmem_st16(t_lane + colS + 16 * c, pk);
+          tmem_st16(t_lane + colS + 16 * c, pk[c]);
         }
         {
           float a0, a1;
           f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
           l += a0 + a1;
-          if (ALIBI) lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[X]);
+        // The sum of the rounded weights, after P has been handed to the tensor core: these adds
+        // (two per pair) lengthened the exponent pass by ~450 cycles when they sat inside it, on
+        // the path from S to P V; here they run while the warp would wait for its next S.
+        {
+          float lr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < C::BN / 32; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) bf16x2_accumulate(lr4[2 * (j & 1)], lr4[2 * (j & 1) + 1], pk[c][j]);
+          lr += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+        }
       }
       if (ROPE && ok) {
         // Look ahead: when the next item with any work has rows in this tile, rotate its Q now
@@ -626,8 +646,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (ok) {
         tc_fence_after();
         const bool store = i < s.Lq;
-        const float nrm = ALIBI ? lr : l;
-        const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
+        const float inv = lr > 0.f ? 1.0f / lr : 0.f;
         if (store && p.lse) p.lse[s.lse_row0 + i] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         // 64 columns of this row of O_X (box bx), normalised and packed to bf16 pairs
         auto load_box = [&](int bx, uint32_t (&ow)[32]) {

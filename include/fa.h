@@ -89,10 +89,13 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
  *   cu_seqlens_q, cu_seqlens_k : device int32 [B + 1], non-decreasing,
  *       cu[0] = 0, cu[B] = total; sequence b owns rows cu[b] .. cu[b+1]-1.
  *   max_seqlen_q / max_seqlen_k : upper bounds of the per-sequence lengths
- *       (the grid is sized from max_seqlen_q; longer sequences are an error the
- *       host cannot see, so the caller must pass true bounds).
+ *       (the grid is sized from max_seqlen_q, so the caller must pass true bounds).
  *   cu_seqlens_q_host : optional host copy of cu_seqlens_q; when given it is
  *       checked (monotone, cu[0] = 0, cu[B] = total_q, lengths <= max_seqlen_q).
+ * The kernel checks every sequence's device entries as well: a sequence whose
+ * cu_seqlens_q/k entries are decreasing, run past total_q/total_k or exceed
+ * max_seqlen_q/k is skipped (no row of it is written) and bit 1 of the device
+ * status word is set (fa_device_status), so bad offsets cannot write outside o/lse.
  */
 FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                         int B, int Hq, int Hkv, int total_q, int total_k,
@@ -170,7 +173,11 @@ FA_API size_t fa_decode_workspace_size(int B, int Hq, int d, int max_splits);
  *       0 .. seqlens_k[b]-1 (the new token's K/V already appended)
  *   lse : [B, Hq] fp32 (may be NULL)
  *   seqlens_k : device int32 [B], values clamped to [0, Ncap]
- *   seqlens_k_host : optional host copy used only to plan the split size
+ *   seqlens_k_host : optional host copy used only to plan the split size; it may
+ *       overstate the device lengths but must not understate them: the plan covers
+ *       max_splits chunks of keys, so keys of a longer device length past them would
+ *       go unread — the combine kernel detects that case and sets bit 1 of the device
+ *       status word (fa_device_status).  Without it the plan assumes Ncap keys.
  *   window : > 0 restricts the query to the last `window` keys
  *   num_splits : 0 = choose automatically; otherwise the maximum number of
  *       key chunks per sequence (each chunk a multiple of 64 keys)
