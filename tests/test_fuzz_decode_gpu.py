@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from fa_workloads import bf16_bits
-from tests._util import check
+from tests._util import abs_bits, check
 
 pytestmark = pytest.mark.gpu
 
@@ -75,13 +75,15 @@ def test_random_decode_matches_oracle(c):
                               num_splits=c["splits"], seqlens_k_host=lens, alibi_slopes=slopes)
     torch.cuda.synchronize()
     rows = oracle.all_rows([nq] * B, Hq)  # (b, h, t)
-    ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(k), bf16_bits(v), [b * nq for b in range(B)], [nq] * B,
-                                   [b * ncap for b in range(B)], lens, scale, True, c["window"], rows,
-                                   alibi_slopes=None if slopes is None else slopes.astype(np.float64))
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    args = ([b * nq for b in range(B)], [nq] * B, [b * ncap for b in range(B)], lens, scale, True, c["window"], rows)
+    sl = None if slopes is None else slopes.astype(np.float64)
+    ro, rl = oracle.attention_rows(qb, kb, vb, *args, alibi_slopes=sl)
+    oa, _ = oracle.attention_rows(qb, kb, abs_bits(vb), *args, alibi_slopes=sl)   # the same weights over |V|
     o4 = o.float().cpu().numpy().reshape(B, nq, Hq, d)
     l3 = lse.cpu().numpy().reshape(B, Hq, nq)
     go = o4[rows[:, 0], rows[:, 2], rows[:, 1]].astype(np.float64)
     gl = l3[rows[:, 0], rows[:, 1], rows[:, 2]].astype(np.float64)
-    check(go, gl, ro, rl, c["name"], strict=False)
+    check(go, gl, ro, rl, c["name"], strict=False, o_abs=oa)
     assert torch.isfinite(o.float()).all()
     assert fa.fa_device_status() == 0
