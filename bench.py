@@ -522,22 +522,43 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
     def prefill_row(name, case, desc, l2, graph=False, **kw):
         x = make_prefill(case)
         q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        o_pre = torch.empty_like(q)
         if case.layout == "packed":
             cu = torch.tensor([0] + list(np.cumsum(x.len_q)), dtype=torch.int32, device=dev)
             host = [0] + [int(c) for c in np.cumsum(x.len_q)]
-            fn = lambda: fa.fa_fwd_varlen(q, k, v, cu, cu, max(x.len_q), max(x.len_k), causal=case.causal,  # noqa
-                                          window=case.window, scale=case.softmax_scale, cu_seqlens_q_host=host)
+            l_pre = torch.empty((case.Hq, q.shape[0]), dtype=torch.float32, device=dev)
+
+            def fn(out=None, lse=None):
+                return fa.fa_fwd_varlen(q, k, v, cu, cu, max(x.len_q), max(x.len_k), causal=case.causal,
+                                        window=case.window, scale=case.softmax_scale, cu_seqlens_q_host=host,
+                                        out=out, lse=lse)
         else:
-            fn = lambda: fa.fa_fwd(q, k, v, causal=case.causal, window=case.window,  # noqa: E731
-                                   scale=case.softmax_scale, **kw)
+            l_pre = torch.empty((case.B, case.Hq, case.Nq), dtype=torch.float32, device=dev)
+
+            def fn(out=None, lse=None):
+                return fa.fa_fwd(q, k, v, causal=case.causal, window=case.window, scale=case.softmax_scale,
+                                 out=out, lse=lse, **kw)
         work = prefill_flops(case, x.len_q, x.len_k)
         add(name, desc, time_alone(fn, steps, warm, stream), work, "TFLOP/s", "tensor", l2)
-        if graph:  # launch-bound: also replay the call from a captured CUDA graph (no host work per call)
+        if graph:
+            # launch-bound: the same call with the outputs allocated once (a serving loop's form: no
+            # allocation per call), its host time per call, and replays of a captured CUDA graph
+            # (no host work per call)
+            pre = lambda: fn(out=o_pre, lse=l_pre)  # noqa: E731
+            ms_pre = time_alone(pre, steps, warm, stream)
+            rows[name]["prealloc_ms_per_call"] = round(ms_pre, 5)
+            torch.cuda.synchronize()
+            n_host = 200
+            t0 = time.perf_counter()
+            for _ in range(n_host):
+                pre()
+            rows[name]["prealloc_host_us_per_call"] = round((time.perf_counter() - t0) / n_host * 1e6, 2)
+            torch.cuda.synchronize()
             reps = 20
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 for _ in range(reps):
-                    fn()
+                    pre()
             g.replay()
             torch.cuda.synchronize()
             (gms,), _ = time_steps([g.replay], max(3, steps // reps), stream)
