@@ -65,6 +65,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of two phases at once: true when both have completed.  The two probes are
+// issued back to back, so their shared-memory round trips overlap.
+__device__ __forceinline__ bool mbar_test2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred q0, q1;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n"
+      " and.pred q0, q0, q1;\n selp.u32 %0, 1, 0, q0;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // sets *abort and the device error word) when the time limit passes or when
 // another thread of the CTA already aborted.

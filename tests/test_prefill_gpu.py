@@ -167,14 +167,19 @@ def test_nan_in_padding_past_seqlens_k_is_ignored(d):
     assert fa.fa_device_status() == 0
 
 
-@pytest.mark.parametrize("d,causal,window", [(128, True, 0), (64, True, 0), (128, False, 0), (64, True, 200)],
-                         ids=["d128_causal", "d64_causal", "d128_noncausal", "d64_window200"])
-def test_rising_scores_move_the_base_on_every_tile(d, causal, window):
-    # Scores that rise along the keys by ~12 log2 units per 128-key tile: every tile's max exceeds
-    # the running max by more than 2^8, so on every tile after a walk's first the exponent base
-    # moves, O is rescaled and the tile's weights are recomputed (on diagonal and window tiles from
-    # re-masked scores).  Neighbouring keys differ by ~0.065 in the exponent, so each row still
-    # spreads its weight over a few dozen keys.
+@pytest.mark.parametrize("d,causal,window,per_key", [(128, True, 0, 0.065), (64, True, 0, 0.065),
+                                                      (128, False, 0, 0.065), (64, True, 200, 0.065),
+                                                      (128, True, 0, 0.26), (64, False, 0, 0.26),
+                                                      (128, True, 300, 0.26)],
+                         ids=["d128_causal", "d64_causal", "d128_noncausal", "d64_window200", "steep_d128_causal",
+                              "steep_d64_noncausal", "steep_d128_window300"])
+def test_rising_scores_move_the_base(d, causal, window, per_key):
+    # Scores that rise along the keys: by ~12 log2 units per 128-key tile (per_key 0.065), so that
+    # the weights of a row grow by 2^12 a tile under a fixed exponent base, or by ~48 (per_key
+    # 0.26), so that within a few tiles a tile's weights would pass 2^57 and the base must move:
+    # the tile's max is taken, O is rescaled and the tile exponentiated again from re-loaded,
+    # re-masked scores (on diagonal and window tiles too).  Each row still spreads its weight
+    # over a few keys.
     case = PrefillCase(f"rising_d{d}", B=1, Hq=4, Hkv=2, Nq=640, Nk=700, d=d, causal=causal, window=window,
                        seed=340 + d)
     x = make_prefill(case)
@@ -182,7 +187,7 @@ def test_rising_scores_move_the_base_on_every_tile(d, causal, window):
     u = torch.randn(d, generator=g)
     u = u / u.norm()
     a = 4.0                                              # query component along u
-    beta = 0.065 / (case.softmax_scale * a)             # key component per position: 0.065 nat per key
+    beta = per_key / (case.softmax_scale * a)           # key component per position: per_key nat per key
     ramp = torch.arange(case.Nk, dtype=torch.float32) * beta
     x.q = (x.q.float() + a * u).to(torch.bfloat16)
     x.k = (x.k.float() * 0.25 + ramp[None, :, None, None] * u).to(torch.bfloat16)
