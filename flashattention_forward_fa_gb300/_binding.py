@@ -8,6 +8,7 @@ import os
 import threading
 from typing import Optional, Sequence, Tuple
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +73,9 @@ def library_path() -> str:
 def load_library():
     """Load libfa_gb300.so (raises if it has not been built)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
@@ -106,11 +110,24 @@ def _stream(t: torch.Tensor):
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
-def _host_ints(x) -> Optional[ctypes.Array]:
+def _host_ints(x):
+    """A host int32 array for the C ABI: None, a contiguous int32 numpy array or CPU tensor (passed
+    by pointer, no copy), or any sequence of ints (copied)."""
     if x is None:
         return None
+    if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags["C_CONTIGUOUS"]:
+        return x.ctypes.data_as(_ip)
+    if isinstance(x, torch.Tensor) and not x.is_cuda and x.dtype == torch.int32 and x.is_contiguous():
+        return ctypes.cast(x.data_ptr(), _ip)
     vals = [int(v) for v in (x.tolist() if isinstance(x, torch.Tensor) else x)]
     return (ctypes.c_int * len(vals))(*vals)
+
+
+def _host_ptr(h):
+    """The _ip pointer of what _host_ints returned."""
+    if h is None or isinstance(h, _ip):
+        return h
+    return ctypes.cast(h, _ip)
 
 
 def alibi_slopes(num_heads: int) -> list:
@@ -266,14 +283,14 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                     Nq=int(max_seqlen_q), Nk=int(max_seqlen_k), d=d, scale=sc, causal=int(bool(causal)),
                     window=int(window), cu_seqlens_q=_ptr(cu_seqlens_q), cu_seqlens_k=_ptr(cu_seqlens_k),
                     total_q=total_q, total_k=total_k,
-                    cu_seqlens_q_host=ctypes.cast(host, _ip) if host is not None else None, alibi_slopes=sp)
+                    cu_seqlens_q_host=_host_ptr(host), alibi_slopes=sp)
         _set_rope(a, rope, rotary_dim, d)
         _check(lib.fa_fwd_ex(ctypes.byref(a), _stream(q)))
         return o, lse
     _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, total_q, total_k,
                              int(max_seqlen_q), int(max_seqlen_k), d, sc, int(bool(causal)), int(window),
                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                             ctypes.cast(host, _ip) if host is not None else None, _stream(q)))
+                             _host_ptr(host), _stream(q)))
     return o, lse
 
 
@@ -285,7 +302,7 @@ def fa_decode_max_splits(B: int, Hq: int, Hkv: int, Ncap: int, window: int = 0, 
                          num_splits: int = 0) -> int:
     host = _host_ints(seqlens_k_host)
     return int(load_library().fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window),
-                                                   ctypes.cast(host, _ip) if host is not None else None,
+                                                   _host_ptr(host),
                                                    int(num_splits)))
 
 
@@ -308,7 +325,7 @@ def fa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq
     Nq = q.shape[1] if q.dim() == 4 else 1
     _, Ncap, Hkv, _ = k_cache.shape
     host = _host_ints(seqlens_k_host)
-    hostp = ctypes.cast(host, _ip) if host is not None else None
+    hostp = _host_ptr(host)
     if workspace is None:
         S = lib.fa_decode_max_splits(B, Hq, Hkv, Ncap, int(window) + Nq - 1 if window > 0 else 0, hostp,
                                      int(num_splits))
@@ -353,7 +370,7 @@ def fa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
     num_pages, page_size, Hkv, _ = k_pages.shape
     max_blocks = block_table.shape[1]
     host = _host_ints(seqlens_k_host)
-    hostp = ctypes.cast(host, _ip) if host is not None else None
+    hostp = _host_ptr(host)
     if workspace is None:
         S = lib.fa_decode_max_splits(B, Hq, Hkv, max_blocks * page_size,
                                      int(window) + Nq - 1 + 63 if window > 0 else 0, hostp, int(num_splits))
@@ -400,7 +417,7 @@ def fa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
     _check(lib.fa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv, Ncap, d,
-                                 sc, int(window), _ptr(seqlens_k), ctypes.cast(host, _ip) if host is not None else None,
+                                 sc, int(window), _ptr(seqlens_k), _host_ptr(host),
                                  int(num_splits), _stream(q)))
     return o, lse
 

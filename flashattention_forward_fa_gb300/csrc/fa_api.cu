@@ -51,10 +51,18 @@ std::mutex g_dev_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+// The last supported device this thread used: repeated calls on one device skip the lock.
+thread_local int t_last_dev = -1;
+thread_local DeviceInfo* t_last_info = nullptr;
+
 fa_status device_info(DeviceInfo** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev == t_last_dev) {
+    *out = t_last_info;
+    return FA_OK;
+  }
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_dev_mu);
   DeviceInfo& di = g_dev[dev];
@@ -72,6 +80,8 @@ fa_status device_info(DeviceInfo** out) {
     di.ready = true;
   }
   if (!di.supported) return fail(FA_ERR_UNSUPPORTED, "device %d is not sm_103 (GB300)", dev);
+  t_last_dev = dev;
+  t_last_info = &di;
   *out = &di;
   return FA_OK;
 }
