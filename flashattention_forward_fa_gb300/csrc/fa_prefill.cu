@@ -37,7 +37,12 @@
 //   reducing their max, unless their weights would sum past 2^57, in which case the
 //   tile's max is taken, O rescaled and the tile exponentiated again.
 //   Per step the issuer waits for the step's V and next K first, then for each P in
-//   turn, so no wait sits between a P and its P V.  The epilogue stages a tile's O
+//   turn, so no wait sits between a P and its P V.  A P reaches the issuer through a
+//   named barrier shared by the tile's four softmax warps and the issuer warp, not an
+//   mbarrier: barrier-unit traffic does not queue behind the S GEMMs' shared-memory
+//   operand reads, which held an mbarrier handoff back by ~450 cycles per tile.  A
+//   named barrier has no time limit, so both sides count their handoffs and, after an
+//   abort, complete the rest without work (handoffs_total).  The epilogue stages a tile's O
 //   in shared memory (64 columns at a time, in the TMA layout) and writes it with
 //   TMA stores; a ragged tile stores row by row.
 //   With ALiBi (jsqmd page, §三 "ALiBi位置编码的线性偏置") each score gets
@@ -64,6 +69,16 @@
 
 namespace fa {
 
+// Threads at a P handoff (named barrier 1 + X): tile X's four softmax warps and the MMA issuer warp.
+constexpr uint32_t kNamedBarThreads = 5 * 32;
+
+// Named barrier `id` (1-15) for `count` threads (a multiple of 32), whole warps converged.
+// Unlike the bounded mbarrier waits it has no time limit: it is used only where every party
+// makes the same number of calls on every path, aborts included.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 template <int D>
 struct PrefillCfg {
   static constexpr int BM = 128;  // query rows per Q tile (one TMEM lane each)
@@ -82,8 +97,8 @@ struct PrefillCfg {
   static constexpr int O_BOX = BM * 64 * 2;
   static constexpr int OFF_BAR = OFF_OST + NQT * O_BOX;
   // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  //           s_full[2], p_full[2], o_final[2], mma_done, q_ready[2], q_empty, o_free[2], o_staged[2]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1 + 2 + 1 + 2 + 2;
+  //           s_full[2], o_final[2], mma_done, q_ready[2], q_empty, o_free[2], o_staged[2]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 2 + 1 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
@@ -263,6 +278,22 @@ __device__ __forceinline__ int snake_item(int k, int n_items) {
   return w < n_items ? (int)w : -1;
 }
 
+// P handoffs of tile X over this CTA's items: one per K/V tile of the tile's walk.  The softmax
+// warps of tile X and the MMA issuer both make exactly this many (named barrier 1 + X).
+template <int BM, int BN>
+__device__ __forceinline__ uint32_t handoffs_total(const PrefillParams& p, int X, int n_rounds, int n_items) {
+  uint32_t n = 0;
+  for (int k = 0; k < n_rounds; ++k) {
+    const int w = snake_item(k, n_items);
+    if (w < 0) continue;
+    const WorkItem it = work_item<BM, BN>(p, w);
+    if (!it.live) continue;
+    const QTileRange r = X ? it.rb : it.ra;
+    if (r.t1 > r.t0) n += (uint32_t)(r.t1 - r.t0);
+  }
+  return n;
+}
+
 // RoPE: rotate Q_X of item `iq` in place once its Q has landed (bar_q phase `ph`) — 16-byte
 // chunks of the 128-byte swizzled rows the TMA wrote, four adjacent pairs per chunk — and tell the
 // MMA issuer (q_ready[X]).  Warp w of the warpgroup takes rows 32 (w & 3) .. 32 (w & 3) + 31, two
@@ -344,8 +375,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint64_t* v_full = k_empty + C::KST;
   uint64_t* v_empty = v_full + C::VST;
   uint64_t* s_full = v_empty + C::VST;  // [2]: one completion per S of tile X
-  uint64_t* p_full = s_full + 2;        // [2]: four warp arrivals per P of tile X
-  uint64_t* o_final = p_full + 2;       // [2]: one completion per item, the last PV of tile X
+  uint64_t* o_final = s_full + 2;       // [2]: one completion per item, the last PV of tile X
   uint64_t* mma_done = o_final + 2;
   uint64_t* q_ready = mma_done + 1;     // [2]: four warp arrivals once Q_X is rotated (RoPE only)
   uint64_t* q_empty = q_ready + 2;      // every S of an item has run: Q may be overwritten
@@ -367,7 +397,6 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);  // one arrival per softmax warp of the tile
       mbar_init(&o_final[i], 1);
     }
     mbar_init(mma_done, 1);
@@ -402,7 +431,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     // the bias below and everything after works on already-scaled scores (xs = 1)
     const float sl2 = p.scale_log2;
     const float xs = ALIBI ? 1.0f : sl2;
-    uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full / p_full phase)
+    uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full phase; P handoffs made)
     uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
     uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
     uint32_t v_next = 0;  // V ring index of the next item's first tile
@@ -485,7 +514,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             // The tile crosses the end of the sequence's keys: the V rows past it are in-bounds
             // memory the caller may leave as anything, and 0 * NaN is NaN in P V.  Zero them (whole
             // 128-byte rows of each slab, so the swizzle does not matter) once V has landed; the
-            // p_full arrival below orders this before the first P V that reads the tile.  Both
+            // P handoff below orders this before the first P V that reads the tile.  Both
             // warpgroups may do it for the same tile; writing zeros over zeros changes nothing.
             const uint32_t g = v_first + (uint32_t)(rev ? it.u1 - 1 - t : t - it.u0);
             ok = __all_sync(0xffffffffu, mbar_wait(&v_full[g % C::VST], (g / C::VST) & 1, abort_flag, p.err));
@@ -636,7 +665,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[X]);
+        named_bar_sync(1 + X, kNamedBarThreads);  // hand P_X(t) to the issuer
       }
       if (ROPE && ok) {
         // Look ahead: when the next item with any work has rows in this tile, rotate its Q now
@@ -737,6 +766,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           }
           if (!store && i < s.rows_out) store_row_zero<D>(p, s, h, i);
         }
+      }
+    }
+    if (!ok) {
+      // Aborted (a wait gave up): the issuer may still be at a P handoff of this tile, and a named
+      // barrier cannot time out, so make the remaining ones without work.
+      const uint32_t total = handoffs_total<C::BM, C::BN>(p, X, n_rounds, n_items);
+      for (; n_sx < total; ++n_sx) {
+        __syncwarp();
+        named_bar_sync(1 + X, kNamedBarThreads);
       }
     }
     if (rg == 0) bulk_wait_all();  // this thread's O stores are complete before the CTA exits
@@ -865,7 +903,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     };
     // O_X (+)= P_X V with V from ring slot g % VST, P_X read from TMEM where the softmax left it.
     // The first P V of an item overwrites O_X: the softmax warps read the previous item's O_X
-    // before they arrived on p_full for this item's first tile, which this issue waited for.
+    // before they handed over P for this item's first tile, which this issue waited for.
     auto issue_pv = [&](int X, int t, uint32_t g, const QTileRange& r) {
       const uint64_t vd = v_desc + (uint64_t)(((g % C::VST) * C::KV_BYTES) >> 4);
       const uint32_t p_cols = tmem + C::COL_S + 128u * X;
@@ -879,7 +917,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     };
     uint32_t gk = 0, gv = 0;              // K / V tiles consumed (ring indices)
     uint32_t n_q = 0;                     // items (bar_q phase)
-    uint32_t n_p[2] = {0, 0};             // P tiles of tile X (p_full phase)
+    uint32_t n_p[2] = {0, 0};             // P handoffs of tile X so far
     uint32_t n_r[2] = {0, 0};             // items with tile X active (q_ready phase)
     bool ok = true;
     for (int k = 0; ok && k < n_rounds; ++k) {
@@ -930,9 +968,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
 #pragma unroll
         for (int X = 0; X < C::NQT; ++X) {
           if (X ? pv_b : pv_a) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&p_full[X], n_p[X] & 1, abort_flag, p.err));
+            __syncwarp();
+            named_bar_sync(1 + X, kNamedBarThreads);  // P_X(t) from the tile's four softmax warps
             ++n_p[X];
-            if (!ok) break;
             tc_fence_after();
             issue_pv(X, t, gvi, X ? it.rb : it.ra);
           }
@@ -945,6 +983,12 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       }
       gk += (uint32_t)(it.u1 - it.u0);
       gv += (uint32_t)(it.u1 - it.u0);
+    }
+    if (!ok) {  // aborted: complete the P handoffs the softmax warps still make (see handoffs_total)
+      const uint32_t ta = handoffs_total<C::BM, C::BN>(p, 0, n_rounds, n_items);
+      const uint32_t tb = handoffs_total<C::BM, C::BN>(p, 1, n_rounds, n_items);
+      for (; n_p[0] < ta; ++n_p[0]) named_bar_sync(1, kNamedBarThreads);
+      for (; n_p[1] < tb; ++n_p[1]) named_bar_sync(2, kNamedBarThreads);
     }
     umma_commit_by(leader, mma_done);  // every MMA issued above has completed once this fires
     mbar_wait_drain(mma_done, 0);
