@@ -525,11 +525,14 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
         o_pre = torch.empty_like(q)
         if case.layout == "packed":
             cu = torch.tensor([0] + list(np.cumsum(x.len_q)), dtype=torch.int32, device=dev)
-            host = [0] + [int(c) for c in np.cumsum(x.len_q)]
+            # the batch's metadata, prepared once as a serving loop holds it: the host copy of
+            # cu_seqlens as an int32 CPU tensor (passed by address) and the maximum lengths as ints
+            host = torch.tensor([0] + [int(c) for c in np.cumsum(x.len_q)], dtype=torch.int32)
+            max_q, max_k = int(max(x.len_q)), int(max(x.len_k))
             l_pre = torch.empty((case.Hq, q.shape[0]), dtype=torch.float32, device=dev)
 
             def fn(out=None, lse=None):
-                return fa.fa_fwd_varlen(q, k, v, cu, cu, max(x.len_q), max(x.len_k), causal=case.causal,
+                return fa.fa_fwd_varlen(q, k, v, cu, cu, max_q, max_k, causal=case.causal,
                                         window=case.window, scale=case.softmax_scale, cu_seqlens_q_host=host,
                                         out=out, lse=lse)
         else:
@@ -554,6 +557,17 @@ def row_measurements(args, dev, stream, peaks, step_inputs):
                 pre()
             rows[name]["prealloc_host_us_per_call"] = round((time.perf_counter() - t0) / n_host * 1e6, 2)
             torch.cuda.synchronize()
+            # back to back: one event pair around n_host calls, as a loop that issues call after
+            # call sees them (the per-call events above add their own host time to every call)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for alloc_name, call in (("b2b_ms_per_call", fn), ("prealloc_b2b_ms_per_call", pre)):
+                torch.cuda.synchronize()
+                ev0.record(stream)
+                for _ in range(n_host):
+                    call()
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                rows[name][alloc_name] = round(ev0.elapsed_time(ev1) / n_host, 5)
             reps = 20
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):

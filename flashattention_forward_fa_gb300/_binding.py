@@ -28,7 +28,7 @@ class FwdArgs(ctypes.Structure):
                 ("B", _i), ("Hq", _i), ("Hkv", _i), ("Nq", _i), ("Nk", _i), ("d", _i),
                 ("scale", _f), ("causal", _i), ("window", _i),
                 ("seqlens_q", _vp), ("seqlens_k", _vp), ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
-                ("total_q", _i), ("total_k", _i), ("cu_seqlens_q_host", _ip), ("alibi_slopes", _vp),
+                ("total_q", _i), ("total_k", _i), ("cu_seqlens_q_host", _vp), ("alibi_slopes", _vp),
                 ("rope_cos", _vp), ("rope_sin", _vp), ("rope_rows", _i), ("rope_dim", _i)]
 
 
@@ -37,22 +37,22 @@ class DecodeArgs(ctypes.Structure):
     _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp),
                 ("B", _i), ("Hq", _i), ("Hkv", _i), ("d", _i), ("scale", _f), ("window", _i), ("Ncap", _i),
                 ("block_table", _vp), ("max_blocks", _i), ("page_size", _i), ("num_pages", _i),
-                ("seqlens_k", _vp), ("seqlens_k_host", _ip), ("num_splits", _i),
+                ("seqlens_k", _vp), ("seqlens_k_host", _vp), ("num_splits", _i),
                 ("workspace", _vp), ("workspace_bytes", _sz), ("alibi_slopes", _vp), ("Nq", _i)]
 
 
 _SIGS = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp]),
-    "fa_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _ip,
+    "fa_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _vp, _vp,
                            _vp]),
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
-    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp, _sz, _vp]),
-    "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _ip, _i]),
-    "fa_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _ip, _i, _vp,
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _vp, _sz, _vp]),
+    "fa_decode_max_splits": (_i, [_i, _i, _i, _i, _i, _vp, _i]),
+    "fa_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _vp, _i, _vp,
                              _sz, _vp]),
     "fa_fwd_ex": (_i, [ctypes.POINTER(FwdArgs), _vp]),
     "fa_decode_ex": (_i, [ctypes.POINTER(DecodeArgs), _vp]),
-    "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _ip, _i, _vp]),
+    "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _vp]),
     "fa_rope": (_i, [_vp, ctypes.c_longlong, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
     "fa_selftest_wait_timeout": (_i, [_i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
@@ -111,23 +111,24 @@ def _stream(t: torch.Tensor):
 
 
 def _host_ints(x):
-    """A host int32 array for the C ABI: None, a contiguous int32 numpy array or CPU tensor (passed
-    by pointer, no copy), or any sequence of ints (copied)."""
+    """A host int32 array for the C ABI: None, a contiguous int32 CPU tensor or numpy array (passed
+    by address, no copy), or any sequence of ints (copied into a ctypes array, which the caller
+    keeps alive until the call returns)."""
     if x is None:
         return None
-    if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags["C_CONTIGUOUS"]:
-        return x.ctypes.data_as(_ip)
     if isinstance(x, torch.Tensor) and not x.is_cuda and x.dtype == torch.int32 and x.is_contiguous():
-        return ctypes.cast(x.data_ptr(), _ip)
-    vals = [int(v) for v in (x.tolist() if isinstance(x, torch.Tensor) else x)]
+        return x.data_ptr()
+    if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags["C_CONTIGUOUS"]:
+        return x.__array_interface__["data"][0]
+    vals = [int(v) for v in (x.tolist() if isinstance(x, (torch.Tensor, np.ndarray)) else x)]
     return (ctypes.c_int * len(vals))(*vals)
 
 
 def _host_ptr(h):
-    """The _ip pointer of what _host_ints returned."""
-    if h is None or isinstance(h, _ip):
+    """The address (or None) of what _host_ints returned, for a void* argument."""
+    if h is None or isinstance(h, int):
         return h
-    return ctypes.cast(h, _ip)
+    return ctypes.addressof(h)
 
 
 def alibi_slopes(num_heads: int) -> list:
@@ -259,7 +260,10 @@ def fa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_
                   return_lse: bool = True, alibi_slopes=None, rope=None, rotary_dim: Optional[int] = None
                   ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Packed varlen prefill.  q [total_q, Hq, d], k/v [total_k, Hkv, d] -> (O, LSE [Hq, total_q]).
-    alibi_slopes, rope, rotary_dim: as for fa_fwd (positions count from each sequence's start)."""
+    alibi_slopes, rope, rotary_dim: as for fa_fwd (positions count from each sequence's start).
+    cu_seqlens_q_host: optional host copy of cu_seqlens_q, checked before the launch; an int32 CPU
+    tensor (or int32 numpy array) is passed by address, the cheapest form for a loop that calls
+    this every step."""
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n)

@@ -96,9 +96,9 @@ struct PrefillCfg {
   static constexpr int OFF_OST = OFF_V + VST * KV_BYTES;
   static constexpr int O_BOX = BM * 64 * 2;
   static constexpr int OFF_BAR = OFF_OST + NQT * O_BOX;
-  // barriers: q, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  //           s_full[2], o_final[2], mma_done, q_ready[2], q_empty, o_free[2], o_staged[2]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 2 + 1 + 2 + 2;
+  // barriers: q[2], k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
+  //           s_full[2], o_final[2], mma_done, q_ready[2], q_empty[2], o_free[2], o_staged[2]
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 2 + 2 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint64_t* bar_q = bars;               // Q of an item landed
-  uint64_t* k_full = bar_q + 1;
+  uint64_t* bar_q = bars;               // [2]: Q_X of an item landed
+  uint64_t* k_full = bar_q + 2;
   uint64_t* k_empty = k_full + C::KST;
   uint64_t* v_full = k_empty + C::KST;
   uint64_t* v_empty = v_full + C::VST;
@@ -378,15 +378,16 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
   uint64_t* o_final = s_full + 2;       // [2]: one completion per item, the last PV of tile X
   uint64_t* mma_done = o_final + 2;
   uint64_t* q_ready = mma_done + 1;     // [2]: four warp arrivals once Q_X is rotated (RoPE only)
-  uint64_t* q_empty = q_ready + 2;      // every S of an item has run: Q may be overwritten
-  uint64_t* o_free = q_empty + 1;       // [2]: tile X's last O store has read its staging buffer
+  uint64_t* q_empty = q_ready + 2;      // [2]: every S of tile X in an item has run: Q_X may be overwritten
+  uint64_t* o_free = q_empty + 2;       // [2]: tile X's last O store has read its staging buffer
   uint64_t* o_staged = o_free + 2;      // [2]: four warp arrivals once a box of tile X's O rows is staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 4);
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(bar_q, 1);
+    mbar_init(&bar_q[0], 1);
+    mbar_init(&bar_q[1], 1);
     for (int i = 0; i < C::KST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -402,7 +403,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     mbar_init(mma_done, 1);
     mbar_init(&q_ready[0], 4);
     mbar_init(&q_ready[1], 4);
-    mbar_init(q_empty, 1);
+    mbar_init(&q_empty[0], 1);
+    mbar_init(&q_empty[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&o_free[i], 1);
       mbar_init(&o_staged[i], 4);
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     const float xs = ALIBI ? 1.0f : sl2;
     uint32_t n_sx = 0;  // S tiles of this warpgroup so far (s_full phase; P handoffs made)
     uint32_t n_ox = 0;  // items in which this tile was active (o_final phase)
-    uint32_t n_q = 0;   // items that loaded Q (bar_q phase)
+    uint32_t n_q = 0;   // items that loaded Q (bar_q[X] phase)
     uint32_t v_next = 0;  // V ring index of the next item's first tile
     uint32_t n_box = 0;   // O boxes of this tile staged and stored so far (o_staged / o_free phase)
     int rot_k = -1;     // RoPE: the round whose item already has this tile's Q rotated
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     // wait more than one phase ahead would pass early), so a tile with no rows in an item still
     // waits its phase.
     auto rotate_q = [&](const WorkItem& iq, uint32_t ph) -> bool {
-      return rotate_q_tile<D>(p, iq, ph, X, warp, lane, sQ, bar_q, q_ready, abort_flag);
+      return rotate_q_tile<D>(p, iq, ph, X, warp, lane, sQ, bar_q + X, q_ready, abort_flag);
     };
     for (int k = 0; ok && k < n_rounds; ++k) {
       const int w = snake_item(k, n_items);
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const uint32_t v_first = v_next;  // V ring index of this item's first tile
       if (it.u1 > it.u0) v_next += (uint32_t)(it.u1 - it.u0);
       if (r.t1 <= r.t0) {  // this tile's rows see no key: O = 0, LSE = -inf (and zero padding rows)
-        if (ROPE && it.u1 > it.u0) ok = __all_sync(0xffffffffu, mbar_wait(bar_q, (n_q - 1) & 1, abort_flag, p.err));
+        if (ROPE && it.u1 > it.u0) ok = __all_sync(0xffffffffu, mbar_wait(bar_q + X, (n_q - 1) & 1, abort_flag, p.err));
         if (ok && i < s.rows_out) store_row_zero<D>(p, s, h, i);
         continue;
       }
@@ -792,18 +794,20 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         if (w < 0) continue;
         const WorkItem it = work_item<C::BM, C::BN>(p, w);
         if (!it.live || it.u1 <= it.u0) continue;
-        // Q of the previous item is in use until its last S has run
-        if (n_q > 0 && !mbar_wait(q_empty, (n_q - 1) & 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar_q, C::NQT * C::Q_BYTES);
 #pragma unroll
-        for (int X = 0; X < C::NQT; ++X)
+        for (int X = 0; X < C::NQT; ++X) {
+          // Q_X of the previous item is in use until tile X's last S has run
+          if (n_q > 0 && !mbar_wait(&q_empty[X], (n_q - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar_q[X], C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, bar_q, c * 64, item_head<C::BM>(p, it, X),
+            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, &bar_q[X], c * 64, item_head<C::BM>(p, it, X),
                         it.s.q_row0 + item_row0<C::BM>(p, it, X));
+        }
+        if (!ok) break;
         ++n_q;
         const int hkv = it.h / p.group;
         // ALiBi walks each item's tiles last to first: bring the next item's Q and first K tiles
@@ -842,7 +846,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
         }
       }
       // drain: every issued load has landed before the CTA may exit
-      if (n_q > 0) mbar_wait_drain(bar_q, (n_q - 1) & 1);
+      if (n_q > 0) {
+        mbar_wait_drain(&bar_q[0], (n_q - 1) & 1);
+        mbar_wait_drain(&bar_q[1], (n_q - 1) & 1);
+      }
       for (uint32_t st = 0; st < (uint32_t)C::KST && st < gk; ++st) {
         const uint32_t last = st + ((gk - 1 - st) / C::KST) * C::KST;
         mbar_wait_drain(&k_full[st], (last / C::KST) & 1);
@@ -916,7 +923,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       if (t == (rev ? r.t0 : r.t1 - 1)) umma_commit_by(leader, &o_final[X]);
     };
     uint32_t gk = 0, gv = 0;              // K / V tiles consumed (ring indices)
-    uint32_t n_q = 0;                     // items (bar_q phase)
+    uint32_t n_q = 0;                     // items (bar_q[X] phase)
     uint32_t n_p[2] = {0, 0};             // P handoffs of tile X so far
     uint32_t n_r[2] = {0, 0};             // items with tile X active (q_ready phase)
     bool ok = true;
@@ -926,22 +933,31 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
       const WorkItem it = work_item<C::BM, C::BN>(p, w);
       if (!it.live || it.u1 <= it.u0) continue;
       const bool act_a = it.ra.t1 > it.ra.t0, act_b = it.rb.t1 > it.rb.t0;
-      ok = mbar_wait(bar_q, n_q & 1, abort_flag, p.err) &&
-           mbar_wait(&k_full[gk % C::KST], (gk / C::KST) & 1, abort_flag, p.err);
+      ok = mbar_wait(&k_full[gk % C::KST], (gk / C::KST) & 1, abort_flag, p.err);
+      const uint32_t qph = n_q & 1;
       ++n_q;
-      if (ROPE) {  // the softmax warps rotate Q in place first
-        if (act_a) ok = ok && mbar_wait(&q_ready[0], n_r[0] & 1, abort_flag, p.err);
-        if (act_b) ok = ok && mbar_wait(&q_ready[1], n_r[1] & 1, abort_flag, p.err);
-        n_r[0] += act_a;
-        n_r[1] += act_b;
+      // Tile A's first S as soon as Q_A (and its rotation) is there, then tile B's.  Tile X's Q
+      // buffer is free once its last S of the item has run; an inactive tile's once its load of
+      // this item has landed (an earlier release would let the next load overlap this one).
+#pragma unroll
+      for (int X = 0; X < C::NQT; ++X) {
+        const bool act = X ? act_b : act_a;
+        const QTileRange& rx = X ? it.rb : it.ra;
+        ok = ok && mbar_wait(&bar_q[X], qph, abort_flag, p.err);
+        if (ROPE && act) ok = ok && mbar_wait(&q_ready[X], n_r[X] & 1, abort_flag, p.err);
+        if (ROPE && act) ++n_r[X];
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (!act) {
+          umma_commit_by(leader, &q_empty[X]);
+        } else if (rev ? rx.t1 == it.u1 : rx.t0 == it.u0) {
+          issue_s(X, gk);
+          if (rx.t1 - rx.t0 == 1) umma_commit_by(leader, &q_empty[X]);
+        }
       }
-      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      if (act_a && (rev ? it.ra.t1 == it.u1 : it.ra.t0 == it.u0)) issue_s(0, gk);
-      if (act_b && (rev ? it.rb.t1 == it.u1 : it.rb.t0 == it.u0)) issue_s(1, gk);
       umma_commit_by(leader, &k_empty[gk % C::KST]);
-      if (it.u1 - it.u0 == 1) umma_commit_by(leader, q_empty);  // every S of the item is issued
       for (int t = rev ? it.u1 - 1 : it.u0; ok && (rev ? t >= it.u0 : t < it.u1); t += rev ? -1 : 1) {
         const int j = rev ? it.u1 - 1 - t : t - it.u0;  // position of tile t in the walk
         const int tn = rev ? t - 1 : t + 1;             // the next tile of the walk
@@ -974,12 +990,15 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             tc_fence_after();
             issue_pv(X, t, gvi, X ? it.rb : it.ra);
           }
-          if (X ? s_b : s_a) issue_s(X, gki + 1);
+          if (X ? s_b : s_a) {
+            issue_s(X, gki + 1);
+            const QTileRange& rx = X ? it.rb : it.ra;
+            if (rev ? tn == rx.t0 : tn == rx.t1 - 1) umma_commit_by(leader, &q_empty[X]);  // tile X's last S
+          }
         }
         if (!ok) break;
         umma_commit_by(leader, &v_empty[gvi % C::VST]);
         if (nxt) umma_commit_by(leader, &k_empty[(gki + 1) % C::KST]);
-        if (rev ? tn == it.u0 : tn == it.u1 - 1) umma_commit_by(leader, q_empty);  // the item's last S is issued
       }
       gk += (uint32_t)(it.u1 - it.u0);
       gv += (uint32_t)(it.u1 - it.u0);
