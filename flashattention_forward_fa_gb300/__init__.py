@@ -18,6 +18,7 @@ Entry points (same names as the C ABI):
   the wrappers above when ``alibi_slopes`` or ``rope`` is given
 * ``fa_device_status()``           read/clear the kernels' error word
 * ``fa_selftest_wait_timeout()``   a wait that runs out on purpose, ending with the timeout bit
+* ``fa_selftest_prefill_abort()``  a prefill whose V loads stop on purpose: its abort path runs
 """
 
 from __future__ import annotations
@@ -36,6 +37,7 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_varlen,
     fa_rope,
+    fa_selftest_prefill_abort,
     fa_selftest_wait_timeout,
     library_path,
     load_library,
@@ -58,6 +60,7 @@ __all__ = [
     "decode_workspace_size",
     "fa_device_status",
     "fa_selftest_wait_timeout",
+    "fa_selftest_prefill_abort",
     "load_library",
     "library_path",
 ]

@@ -55,6 +55,7 @@ _SIGS = {
     "fa_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _vp]),
     "fa_rope": (_i, [_vp, ctypes.c_longlong, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
     "fa_selftest_wait_timeout": (_i, [_i, _vp]),
+    "fa_selftest_prefill_abort": (_i, [ctypes.POINTER(FwdArgs), _i, _vp]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_device_status": (_i, [ctypes.POINTER(ctypes.c_uint32), _i]),
 }
@@ -431,6 +432,26 @@ def fa_selftest_wait_timeout(limit_ms: int = 20, stream=None) -> None:
     afterwards fa_device_status() shows the timeout bit (1)."""
     s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
     _check(load_library().fa_selftest_wait_timeout(int(limit_ms), ctypes.c_void_p(s)))
+
+
+def fa_selftest_prefill_abort(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, v_loads: int, causal: bool = False,
+                              window: int = 0, alibi_slopes=None, rope=None) -> None:
+    """The prefill of fa_fwd on padded q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d] with every CTA's V
+    loads cut off after v_loads tiles: the kernel's abort path runs (its waits give up after 2 s)
+    and fa_device_status() shows the timeout bit (1).  The outputs are discarded."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    keep, sp = _slopes_ptr(alibi_slopes, Hq, q.device)
+    a = FwdArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), o=_ptr(o), lse=_ptr(lse), B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nk=Nk, d=d,
+                scale=1.0 / math.sqrt(d), causal=int(bool(causal)), window=int(window), alibi_slopes=sp)
+    _set_rope(a, rope, None, d)
+    _check(lib.fa_selftest_prefill_abort(ctypes.byref(a), int(v_loads), _stream(q)))
+    torch.cuda.synchronize(q.device)  # o, lse and the slopes stay alive until the kernel has ended
 
 
 def fa_device_status(clear: bool = True) -> int:

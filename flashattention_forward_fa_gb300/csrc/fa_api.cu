@@ -166,13 +166,27 @@ fa_status check_common(const void* q, const void* k, const void* v, void* o, con
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// fa_fwd_ex with, for the abort self-test, a cap on each CTA's V loads (0: none).
+fa_status fwd_impl(const fa_fwd_args* a, int v_load_cap, fa_stream_t stream);
+
 }  // namespace
 
 extern "C" {
 
 const char* fa_last_error(void) { return g_last_error.c_str(); }
 
-fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
+fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) { return fwd_impl(a, 0, stream); }
+
+fa_status fa_selftest_prefill_abort(const fa_fwd_args* a, int v_loads, fa_stream_t stream) {
+  if (v_loads <= 0) return fail(FA_ERR_INVALID, "v_loads must be positive");
+  return fwd_impl(a, v_loads, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+fa_status fwd_impl(const fa_fwd_args* a, int v_load_cap, fa_stream_t stream) {
   if (!a) return fail(FA_ERR_INVALID, "args must be non-null");
   const int B = a->B, Hq = a->Hq, Hkv = a->Hkv, d = a->d, window = a->window;
   fa_status st = check_common(a->q, a->k, a->v, a->o, a->lse, B, Hq, Hkv, d, a->scale);
@@ -255,10 +269,15 @@ fa_status fa_fwd_ex(const fa_fwd_args* a, fa_stream_t stream) {
     p.rope_rows = a->rope_rows;
     p.rope_dim = a->rope_dim;
   }
+  p.v_load_cap = v_load_cap;
   cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, max_rows, di->sm_count, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return FA_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                  int Nk, int d, float scale, int causal, int window, const int* seqlens_q, const int* seqlens_k,

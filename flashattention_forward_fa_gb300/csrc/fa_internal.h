@@ -27,6 +27,7 @@ struct PrefillParams {
   int rope_rows, rope_dim;
   int n_qblk;              // row blocks per sequence (set by the launcher)
   int pair_heads;          // items pair two query heads of one KV group (set by the launcher)
+  int v_load_cap;          // > 0: each CTA's V producer issues only this many loads (the abort self-test)
 };
 
 struct RopeParams {

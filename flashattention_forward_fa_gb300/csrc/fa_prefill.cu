@@ -874,6 +874,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
             ok = false;
             break;
           }
+          if (p.v_load_cap > 0 && gv >= (uint32_t)p.v_load_cap) {  // abort self-test: V stops coming
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
           uint8_t* dst = sV + st * C::KV_BYTES;
           const int row = it.s.k_row0 + t * C::BN;

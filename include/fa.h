@@ -309,6 +309,18 @@ FA_API const char* fa_last_error(void);
 FA_API fa_status fa_selftest_wait_timeout(int limit_ms, fa_stream_t stream);
 
 /*
+ * Diagnostic: fa_fwd_ex in which every CTA's V producer stops after v_loads (> 0) tile loads, so
+ * the MMA issuer's wait for the next V tile gives up after the kernels' 2 s limit.  Every role then
+ * unwinds: the waits of the others end on the abort flag, the P handoffs between the softmax warps
+ * and the issuer (named barriers, which have no time limit) are completed without work by both
+ * sides, copies and MMAs in flight are waited for, TMEM is freed and the kernel returns with bit 0
+ * of the device status word set.  Outputs are then undefined.  The check that the abort path of the
+ * prefill kernel ends instead of hanging; a problem whose CTAs need at most v_loads V tiles each
+ * completes normally.  Asynchronous on `stream`; FA_ERR_INVALID for v_loads <= 0 and as fa_fwd_ex.
+ */
+FA_API fa_status fa_selftest_prefill_abort(const fa_fwd_args* args, int v_loads, fa_stream_t stream);
+
+/*
  * Read (and optionally clear) the device status word of the current device:
  * bit 0 = some kernel wait passed its time limit, bit 1 = a device-side bounds
  * check fired.  Synchronises the device.  Returns FA_ERR_TIMEOUT when bits

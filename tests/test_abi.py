@@ -232,3 +232,13 @@ def test_selftest_wait_timeout_arguments_checked(lib):
     L = b.load_library()
     assert L.fa_selftest_wait_timeout(0, None) == 1
     assert L.fa_selftest_wait_timeout(5000, None) == 1 and b"limit_ms" in L.fa_last_error()
+
+
+def test_selftest_prefill_abort_arguments_checked(lib):
+    _, b = _binding()
+    L = b.load_library()
+    a = b.FwdArgs()
+    assert L.fa_selftest_prefill_abort(ctypes.byref(a), 0, None) == 1 and b"v_loads" in L.fa_last_error()
+    assert L.fa_selftest_prefill_abort(None, 2, None) == 1 and b"non-null" in L.fa_last_error()
+    # otherwise the arguments go through the same checks as fa_fwd_ex (here: null tensors)
+    assert L.fa_selftest_prefill_abort(ctypes.byref(a), 2, None) == 1

@@ -28,3 +28,36 @@ def test_wait_that_never_completes_reports_timeout_and_context_survives():
     ro, rl = oracle_prefill_rows(x, rows)
     check(go, gl, ro, rl, case.name)
     assert fa.fa_device_status() == 0
+
+
+# The prefill kernel's own abort path: each CTA's V loads stop after two tiles, so the MMA
+# issuer's wait for the third gives up (2 s) and every role unwinds — including the P handoffs,
+# named barriers without a time limit that both sides complete without work.  The kernel must
+# end with the timeout bit, and a normal prefill right after it must match the oracle.
+ABORT_CASES = [
+    dict(name="abort_d128_causal", B=1, Hq=4, Hkv=4, Nq=1024, Nk=1024, d=128, causal=True),
+    dict(name="abort_d64_alibi_gqa", B=2, Hq=8, Hkv=2, Nq=640, Nk=640, d=64, causal=False, alibi=True),
+    dict(name="abort_d128_window_rope", B=1, Hq=4, Hkv=2, Nq=900, Nk=900, d=128, causal=True, window=300,
+         rope=True),
+]
+
+
+@pytest.mark.parametrize("cfg", ABORT_CASES, ids=[c["name"] for c in ABORT_CASES])
+def test_prefill_abort_path_ends_with_timeout_and_context_survives(cfg):
+    import flashattention_forward_fa_gb300 as fa
+    case = PrefillCase(cfg["name"], B=cfg["B"], Hq=cfg["Hq"], Hkv=cfg["Hkv"], Nq=cfg["Nq"], Nk=cfg["Nk"],
+                       d=cfg["d"], causal=cfg["causal"], window=cfg.get("window", 0), seed=611)
+    x = make_prefill(case)
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    slopes = fa.alibi_slopes(case.Hq) if cfg.get("alibi") else None
+    rope = fa.rope_tables(case.Nk, case.d, device="cuda") if cfg.get("rope") else None
+    fa.fa_device_status(clear=True)
+    fa.fa_selftest_prefill_abort(q, k, v, 2, causal=case.causal, window=case.window, alibi_slopes=slopes, rope=rope)
+    assert fa.fa_device_status(clear=True) & 1, "the stalled prefill did not report a timeout"
+    o, lse = fa.fa_fwd(q, k, v, causal=case.causal, window=case.window)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    rows = sample_rows(x, 48)
+    go, gl = gather_prefill_rows(x, o, lse, rows)
+    ro, rl = oracle_prefill_rows(x, rows)
+    check(go, gl, ro, rl, case.name)
