@@ -1031,7 +1031,10 @@ template <int D, bool ALIBI, bool ROPE, bool PADK>
 static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                                     const PrefillParams& p, int max_rows, int sm_count, cudaStream_t stream) {
   using C = PrefillCfg<D>;
-  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.  The
+  // register split (setmaxnreg) must fit in the registers the block is launched with: a split
+  // above them would make the softmax warps wait for registers forever, so a build whose launch
+  // register count came out lower than the split needs is refused here instead of launched.
   static int attr_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1040,6 +1043,11 @@ static cudaError_t launch_prefill_d(const CUtensorMap& tq, const CUtensorMap& tk
     e = cudaFuncSetAttribute(fa_prefill_kernel<D, ALIBI, ROPE, PADK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, fa_prefill_kernel<D, ALIBI, ROPE, PADK>);
+    if (e != cudaSuccess) return e;
+    if ((long long)fa.numRegs * C::THREADS < 2LL * 128 * C::REGS_SOFTMAX + 128LL * C::REGS_PRODUCER)
+      return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   // Persistent (one CTA per SM walks its share of the items) when every sequence has the same
