@@ -50,6 +50,7 @@ METRIC = "attention fwd TFLOP/s (prefill) & decode GB/s on 1 GB300, % of rooflin
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_NOTE = "inputs larger than L2 (prefill Q/K/V/O 256 MB, decode K/V cache 2.1 GB); no flush"
 PREFILL_KERNEL_SOURCES = ["flashattention_forward_fa_gb300/csrc/fa_prefill.cu",
+                          "flashattention_forward_fa_gb300/csrc/fa_items.cuh",
                           "flashattention_forward_fa_gb300/csrc/sm103_ptx.cuh"]
 DECODE_KERNEL_SOURCES = ["flashattention_forward_fa_gb300/csrc/fa_decode.cu",
                          "flashattention_forward_fa_gb300/csrc/sm103_ptx.cuh"]
