@@ -14,12 +14,12 @@
 //   one sequence that read the same K/V: consecutive row tiles of one query head, or,
 //   with an even number of query heads per KV head, the same rows of two heads of one
 //   group (identical K/V ranges and masks).  The K/V rings and every barrier phase run on across
-//   items, so the next item's Q load, K/V loads and first S overlap the current
-//   item's last P V and epilogue instead of a CTA launch, TMEM allocation and
-//   pipeline fill per item.  12 warps:
+//   items, so the next item's Q load (each tile's Q as soon as that tile's last S of the
+//   current item has run), K/V loads and first S overlap the current item's last P V and
+//   epilogue instead of a CTA launch, TMEM allocation and pipeline fill per item.  12 warps:
 //     warps 0-3   softmax of tile A: thread r owns score row r (TMEM lane r)
 //     warps 4-7   softmax of tile B
-//     warp  8     TMA producer for Q (once) and the K ring
+//     warp  8     TMA producer for Q (each tile's Q once per item) and the K ring
 //     warp  9     TMA producer for the V ring
 //     warp  10    TMEM allocator and tcgen05.mma issuer
 //     warp  11    idle (gives its registers to the softmax warpgroups)
