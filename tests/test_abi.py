@@ -242,3 +242,25 @@ def test_selftest_prefill_abort_arguments_checked(lib):
     assert L.fa_selftest_prefill_abort(None, 2, None) == 1 and b"non-null" in L.fa_last_error()
     # otherwise the arguments go through the same checks as fa_fwd_ex (here: null tensors)
     assert L.fa_selftest_prefill_abort(ctypes.byref(a), 2, None) == 1
+
+
+def test_host_int_arrays_reach_the_library_by_address():
+    """A host int32 copy (cu_seqlens_q_host, seqlens_k_host) is handed to the C ABI as an address:
+    a contiguous int32 CPU tensor or numpy array without a copy, any other sequence copied into a
+    ctypes array that the caller keeps alive; the address reads back the same values."""
+    import numpy as np
+    import torch
+    _, b = _binding()
+    vals = [0, 5, 17, 300, 301, 1024]
+    t = torch.tensor(vals, dtype=torch.int32)
+    a = np.array(vals, dtype=np.int32)
+    for src, no_copy in ((t, True), (a, True), (vals, False), (torch.tensor(vals), False), (np.array(vals), False)):
+        h = b._host_ints(src)
+        addr = b._host_ptr(h)
+        assert isinstance(addr, int) and addr != 0
+        got = list((ctypes.c_int * len(vals)).from_address(addr))
+        assert got == vals, (type(src), got)
+        if no_copy:
+            expect = src.data_ptr() if isinstance(src, torch.Tensor) else src.__array_interface__["data"][0]
+            assert addr == expect
+    assert b._host_ints(None) is None and b._host_ptr(None) is None
