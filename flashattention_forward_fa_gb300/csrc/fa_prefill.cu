@@ -70,6 +70,31 @@
 
 namespace fa {
 
+// TMA load with an L2 eviction-priority hint (a policy from createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                 int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], "
+      "[%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy(bool keep) {
+  uint64_t p;
+  if (keep) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// The producers' loads: with ALiBi (items walk their tiles last to first) K and V are marked to
+// stay in L2 and Q to leave it first (measured 2.7 % faster there; neutral to 1 % slower on
+// forward walks, which keep the plain loads).
+template <bool HINT>
+__device__ __forceinline__ void tma_load_3d_walk(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  if (HINT) tma_load_3d_hint(dst, map, bar, c0, c1, c2, policy);
+  else tma_load_3d(dst, map, bar, c0, c1, c2);
+}
+
 // Threads at a P handoff (named barrier 1 + X): tile X's four softmax warps and the MMA issuer warp.
 constexpr uint32_t kNamedBarThreads = 5 * 32;
 
@@ -635,6 +660,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
+      const uint64_t pol_kv = ALIBI ? l2_policy(true) : 0, pol_q = ALIBI ? l2_policy(false) : 0;
       uint32_t gk = 0;   // K tiles issued (ring index)
       uint32_t n_q = 0;  // items whose Q was loaded
       bool ok = true;
@@ -653,8 +679,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           mbar_arrive_expect_tx(&bar_q[X], C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, &bar_q[X], c * 64, item_head<C::BM>(p, it, X),
-                        it.s.q_row0 + item_row0<C::BM>(p, it, X));
+            tma_load_3d_walk<ALIBI>(sQ + X * C::Q_BYTES + c * C::CHUNK, &tm_q, &bar_q[X], c * 64,
+                                    item_head<C::BM>(p, it, X), it.s.q_row0 + item_row0<C::BM>(p, it, X), pol_q);
         }
         if (!ok) break;
         ++n_q;
@@ -691,7 +717,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           uint8_t* dst = sK + st * C::KV_BYTES;
           const int row = it.s.k_row0 + t * C::BN;
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_k, &k_full[st], c * 64, hkv, row);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_walk<ALIBI>(dst + c * C::CHUNK, &tm_k, &k_full[st], c * 64, hkv, row, pol_kv);
         }
       }
       // drain: every issued load has landed before the CTA may exit
@@ -709,6 +736,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
     setmaxnreg_dec<REGS_P>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = ALIBI ? l2_policy(true) : 0;
       uint32_t gv = 0;  // V tiles issued (ring index)
       bool ok = true;
       for (int k = 0; ok && k < n_rounds; ++k) {
@@ -731,7 +759,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           uint8_t* dst = sV + st * C::KV_BYTES;
           const int row = it.s.k_row0 + t * C::BN;
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_v, &v_full[st], c * 64, hkv, row);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_walk<ALIBI>(dst + c * C::CHUNK, &tm_v, &v_full[st], c * 64, hkv, row, pol_kv);
         }
       }
       for (uint32_t st = 0; st < (uint32_t)C::VST && st < gv; ++st) {
