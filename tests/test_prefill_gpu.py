@@ -170,16 +170,19 @@ def test_nan_in_padding_past_seqlens_k_is_ignored(d):
 @pytest.mark.parametrize("d,causal,window,per_key", [(128, True, 0, 0.065), (64, True, 0, 0.065),
                                                       (128, False, 0, 0.065), (64, True, 200, 0.065),
                                                       (128, True, 0, 0.26), (64, False, 0, 0.26),
-                                                      (128, True, 300, 0.26)],
+                                                      (128, True, 300, 0.26), (128, True, 0, 0.42),
+                                                      (64, False, 0, 0.42), (128, True, 300, 0.42)],
                          ids=["d128_causal", "d64_causal", "d128_noncausal", "d64_window200", "steep_d128_causal",
-                              "steep_d64_noncausal", "steep_d128_window300"])
+                              "steep_d64_noncausal", "steep_d128_window300", "half2_d128_causal",
+                              "half2_d64_noncausal", "half2_d128_window300"])
 def test_rising_scores_move_the_base(d, causal, window, per_key):
     # Scores that rise along the keys: by ~12 log2 units per 128-key tile (per_key 0.065), so that
     # the weights of a row grow by 2^12 a tile under a fixed exponent base, or by ~48 (per_key
     # 0.26), so that within a few tiles a tile's weights would pass 2^57 and the base must move:
-    # the tile's max is taken, O is rescaled and the tile exponentiated again from re-loaded,
-    # re-masked scores (on diagonal and window tiles too).  Each row still spreads its weight
-    # over a few keys.
+    # the tile's max is taken, O is rescaled and the tile exponentiated again from the scores
+    # (on diagonal and window tiles too).  At ~0.6 log2 units per key (per_key 0.42) the first
+    # 64 keys of a tile stay below the limit and only the last 64 pass it.  Each row still
+    # spreads its weight over a few keys.
     case = PrefillCase(f"rising_d{d}", B=1, Hq=4, Hkv=2, Nq=640, Nk=700, d=d, causal=causal, window=window,
                        seed=340 + d)
     x = make_prefill(case)
