@@ -535,6 +535,8 @@ fa_status fa_rope(void* x, long long rows, int heads, int d, int rotary_dim, con
   if (rotary_dim <= 0 || rotary_dim % 8 != 0 || rotary_dim > d)
     return fail(FA_ERR_INVALID, "rotary_dim (%d) must be a positive multiple of 8, at most d", rotary_dim);
   if (d % 8 != 0) return fail(FA_ERR_INVALID, "d must be a multiple of 8");
+  if (rotary_dim > 1024) return fail(FA_ERR_UNSUPPORTED, "rotary_dim (%d) above 1024", rotary_dim);
+  if ((long long)heads * d > 0x7fffffffLL) return fail(FA_ERR_INVALID, "heads x d must fit in 31 bits");
   if (!aligned16(x) || !aligned16(cos_t) || !aligned16(sin_t))
     return fail(FA_ERR_INVALID, "x and the tables must be 16-byte aligned");
   if (rows == 0) return FA_OK;

@@ -153,8 +153,9 @@ FA_API fa_status fa_fwd_ex(const fa_fwd_args* args, fa_stream_t stream);
  * int32 [rows]) — pairs of adjacent dimensions (2j, 2j+1), j < rotary_dim / 2, by
  * cos_t / sin_t [table_rows, rotary_dim / 2] (device fp32), fp32 math, bf16
  * round-to-nearest-even result; dimensions >= rotary_dim are untouched.
- * rotary_dim: multiple of 8, <= d.  A position outside [0, table_rows) leaves its
- * row unchanged and sets bit 1 of the device status word.
+ * rotary_dim: multiple of 8, <= d (FA_ERR_INVALID otherwise) and <= 1024
+ * (FA_ERR_UNSUPPORTED above); heads x d below 2^31.  A position outside
+ * [0, table_rows) leaves its row unchanged and sets bit 1 of the device status word.
  */
 FA_API fa_status fa_rope(void* x, long long rows, int heads, int d, int rotary_dim, const int* positions,
                          const float* cos_t, const float* sin_t, int table_rows, fa_stream_t stream);

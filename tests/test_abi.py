@@ -212,6 +212,8 @@ def test_rope_arguments_checked(lib):
     assert L.fa_rope(d, -1, 2, 64, 64, d, d, d, 8, None) == 1
     assert L.fa_rope(d, 4, 2, 64, 64, d, d + 8, d, 8, None) == 1 and b"aligned" in L.fa_last_error()
     assert L.fa_rope(d, 0, 2, 64, 64, d, d, d, 8, None) == 0                  # nothing to do
+    assert L.fa_rope(d, 4, 2, 2048, 1032, d, d, d, 8, None) == 2 and b"1024" in L.fa_last_error()
+    assert L.fa_rope(d, 4, 1 << 20, 4096, 64, d, d, d, 8, None) == 1 and b"31 bits" in L.fa_last_error()
 
 
 def test_rope_tables_match_oracle_tables():

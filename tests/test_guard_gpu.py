@@ -154,17 +154,17 @@ def test_decode_writes_stay_inside_outputs_and_workspace(nq, paged):
     assert fa.fa_device_status() == 0
 
 
-def test_rope_writes_stay_inside_its_tensor():
+@pytest.mark.parametrize("rows,H,d,rd", [(1000, 2, 128, 64), (257, 40, 128, 120)])  # narrow and wide rows
+def test_rope_writes_stay_inside_its_tensor(rows, H, d, rd):
     import flashattention_forward_fa_gb300 as fa
-    rows, H, d = 1000, 2, 128
     g = torch.Generator("cpu").manual_seed(912)
     x = torch.randn(rows, H, d, generator=g).to(torch.bfloat16)
     gx = Guarded((rows, H, d), torch.bfloat16, 4096)
     gx.t.copy_(x.cuda())
     pos = torch.arange(rows, dtype=torch.int32, device="cuda")
-    fa.fa_rope(gx.t, pos, fa.rope_tables(rows, 64, device="cuda"))
+    fa.fa_rope(gx.t, pos, fa.rope_tables(rows, rd, device="cuda"))
     gx.assert_margins_intact("fa_rope")
-    assert torch.equal(gx.t[..., 64:].cpu(), x[..., 64:])
+    assert torch.equal(gx.t[..., rd:].cpu(), x[..., rd:])
     assert fa.fa_device_status() == 0
 
 

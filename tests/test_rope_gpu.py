@@ -24,7 +24,11 @@ def _bf16_pattern_value(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("rows,H,d,rd", [(1000, 8, 128, 128), (333, 2, 64, 64), (77, 4, 128, 64), (5, 1, 64, 8)])
+# The first four shapes run the one-thread-per-chunk form of the kernel, the last three (rows of
+# at least 512 16-byte chunks) the one-row-per-CTA form, including 15 chunks per head (threads
+# past the last whole group idle) and a row that takes one pass of four heads per thread.
+@pytest.mark.parametrize("rows,H,d,rd", [(1000, 8, 128, 128), (333, 2, 64, 64), (77, 4, 128, 64), (5, 1, 64, 8),
+                                         (300, 32, 128, 128), (129, 40, 128, 120), (64, 64, 64, 64)])
 def test_rope_kernel_matches_oracle(rows, H, d, rd):
     # Tolerance derived from the kernel's arithmetic.  The kernel rotates a pair (x, y) in fp32 as
     # fma(x, c, -(y s)) and fma(x, s, y c) with the fp32 table values c, s, then rounds to bf16
@@ -65,15 +69,17 @@ def test_rope_kernel_matches_oracle(rows, H, d, rd):
     assert fa.fa_device_status() == 0
 
 
-def test_rope_position_out_of_table_reported():
+@pytest.mark.parametrize("H,d", [(2, 64), (32, 128)])
+def test_rope_position_out_of_table_reported(H, d):
     import flashattention_forward_fa_gb300 as fa
-    x = torch.randn(4, 2, 64).to(torch.bfloat16).cuda()
+    x = torch.randn(4, H, d).to(torch.bfloat16).cuda()
     x0 = x.clone()
     pos = torch.tensor([0, 1, 99, 2], dtype=torch.int32, device="cuda")
     fa.fa_device_status(clear=True)
-    fa.fa_rope(x, pos, _tables(16, 64))
+    fa.fa_rope(x, pos, _tables(16, d))
     assert fa.fa_device_status(clear=True) & 2
     assert torch.equal(x[2], x0[2])
+    assert not torch.equal(x[3], x0[3])  # the rows around it are still rotated
 
 
 def _oracle_rope_prefill(x, case, cos64, sin64, rd):
