@@ -467,40 +467,88 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS, 1)
           ts = exp_tile(m, &tlr);
           done = __all_sync(0xffffffffu, ts <= 0x1p57f);  // false for inf / NaN too
         }
-        if (!done) {
-          float mx;
-          if (ALIBI) {
-            // ALiBi (bias -m_h |p - j|, log2 units).  When every key of the tile lies on one side
-            // of p — always for causal rows, whose later keys are masked — the bias is linear in
-            // the key, b_j = ba j + bc: it is added inside the exponent's FMA by eight chains of
-            // paired adds, and the row max is bounded per 16-key chunk (scaled raw chunk max plus
-            // the chunk's largest bias).  The bound exceeds the biased max by at most 15 |ba|
-            // (below 19 for the steepest slope), which only lowers every weight of the tile by a
-            // common factor, and it keeps the bias off the max's critical path.  A tile that p
-            // splits (non-causal only) takes |.| per key before the max.
-            const int dk = pos - k0;
+        if constexpr (ALIBI) {
+          // ALiBi (bias -m_h |p - j|, log2 units).  When every key of the tile lies on one side of
+          // p — always for causal rows, whose later keys are masked — the bias is linear in the
+          // key, b_j = ba j + bc: it is added inside the exponent's FMA by eight chains of paired
+          // adds, and a max, where one is taken, is bounded per 16-key chunk (scaled raw chunk max
+          // plus the chunk's largest bias).  The bound exceeds the biased max by at most 15 |ba|
+          // (below 19 for the steepest slope), which only lowers every weight of the tile by a
+          // common factor, and it keeps the bias off the max's critical path.  A tile that p
+          // splits (non-causal only) takes |.| per key before the max.  Linear tiles of a row
+          // with a base go first without a max, as above: the walk starts at the diagonal, whose
+          // tile sets the base, so later tiles rarely need one (3-4 % faster).  One
+          // exponentiation site, in a loop of at most two passes (a second copy spilled); the
+          // generic path below is then skipped.
+          const int dk = pos - k0;
+          bool quick = __all_sync(0xffffffffu, (p.causal || dk >= C::BN - 1 || dk <= 0) && m != -INFINITY);
+#pragma unroll 1
+          for (;;) {
+            float mx;
             lin = p.causal || dk >= C::BN - 1 || dk <= 0;
             if (lin) {
               ba = (p.causal || dk > 0) ? slope2 : -slope2;
               bc = -ba * (float)dk;
               xs_t = sl2;
-              const float jtop = ba >= 0.f ? 15.f : 0.f;  // key of a chunk's largest bias
-              float c8[C::BN / 16];
-#pragma unroll
-              for (int q = 0; q < C::BN / 16; ++q) {
-                const float* v = sc + 16 * q;
-                const float c16 = fmax3(fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmax3(v[6], v[7], v[8])),
-                                        fmax3(v[9], v[10], v[11]), fmax3(fmax3(v[12], v[13], v[14]), v[15], v[15]));
-                c8[q] = fmaf(c16, sl2, fmaf(ba, (float)(16 * q) + jtop, bc));
-              }
-              mx = fmax3(fmax3(c8[0], c8[1], c8[2]), fmax3(c8[3], c8[4], c8[5]), fmaxf(c8[6], c8[7]));
-            } else {
-              const float dpos = (float)dk;
-#pragma unroll
-              for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
             }
+            if (!quick) {
+              if (lin) {
+                const float jtop = ba >= 0.f ? 15.f : 0.f;  // key of a chunk's largest bias
+                float c8[C::BN / 16];
+#pragma unroll
+                for (int q = 0; q < C::BN / 16; ++q) {
+                  const float* v = sc + 16 * q;
+                  const float c16 = fmax3(fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmax3(v[6], v[7], v[8])),
+                                          fmax3(v[9], v[10], v[11]), fmax3(fmax3(v[12], v[13], v[14]), v[15], v[15]));
+                  c8[q] = fmaf(c16, sl2, fmaf(ba, (float)(16 * q) + jtop, bc));
+                }
+                mx = fmax3(fmax3(c8[0], c8[1], c8[2]), fmax3(c8[3], c8[4], c8[5]), fmaxf(c8[6], c8[7]));
+              } else {
+                const float dpos = (float)dk;
+#pragma unroll
+                for (int j = 0; j < C::BN; ++j) sc[j] = fmaf(sc[j], sl2, -slope2 * fabsf(dpos - (float)j));
+                float t8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
+#pragma unroll
+                for (int j = 24; j < C::BN - 8; j += 16)
+#pragma unroll
+                  for (int u = 0; u < 8; ++u) t8[u] = fmax3(t8[u], sc[j + u], sc[j + 8 + u]);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t8[u] = fmaxf(t8[u], sc[C::BN - 8 + u]);
+                mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+              }
+              const float m_new = fmaxf(m, mx);
+              const bool need = m_new > m + 8.0f;
+              const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+              const bool o_live = need && (n > 0) && (m != -INFINITY);
+              if (__any_sync(0xffffffffu, o_live)) {
+                const float f = o_live ? alpha : 1.0f;
+#pragma unroll
+                for (int c = 0; c < D; c += 16) {
+                  uint32_t ov[16];
+                  tmem_ld16(t_lane + colO + c, ov);
+                  tmem_ld_wait(ov);
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                  tmem_st16(t_lane + colO + c, ov);
+                }
+              }
+              if (need) {
+                l *= alpha;
+                lr *= alpha;
+                m = m_new;
+              }
+            }
+            ts = exp_tile((m == -INFINITY) ? 0.f : m, &tlr);
+            if (!quick || __all_sync(0xffffffffu, ts <= 0x1p57f)) break;
+            quick = false;
           }
-          if (!lin) {  // row max: eight independent chains of three-input max
+          done = true;
+        }
+        if (!done) {
+          float mx;
+          {  // row max: eight independent chains of three-input max
             float t8[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) t8[u] = fmax3(sc[u], sc[8 + u], sc[16 + u]);
