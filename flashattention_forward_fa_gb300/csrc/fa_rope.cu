@@ -13,8 +13,8 @@
 // thread takes one chunk position (four pairs) in four heads of the row and loads all four
 // before storing any, so it keeps 64 bytes in flight and reads one float4 of each table per row
 // (L2-resident), with 32-bit index arithmetic within the row.  Narrower rows, where that would
-// leave threads idle or with one chunk each: one thread per 16-byte chunk over the whole
-// tensor (grid-stride), with its row's position and table entries.
+// leave threads idle or with one chunk each: two 16-byte chunks per thread over the flat chunk
+// index of the whole tensor (grid-stride), each with its row's position and table entries.
 // The prefill kernel rotates Q itself after loading it; this pass is for K (rotated once, as
 // it is when written to a KV cache) or for any tensor a caller wants rotated.
 #include <cuda_bf16.h>
@@ -26,26 +26,42 @@
 
 namespace fa {
 
-// Narrow rows: one thread per 16-byte chunk of the tensor.
+// Narrow rows: two 16-byte chunks of the flat chunk index per thread (idx and idx + stride), both
+// loaded before either is stored; 32-bit index arithmetic when the tensor has fewer than 2^31
+// chunks.
+template <typename Idx>
 __global__ void __launch_bounds__(256) fa_rope_flat_kernel(RopeParams p) {
   const int chunks = p.rotary_dim / 8;  // 16-byte chunks of the rotated part of a row and head
-  const long long total = (long long)p.rows * p.heads * chunks;
+  const Idx per_row = (Idx)p.heads * (Idx)chunks;
+  const Idx total = (Idx)p.rows * per_row;
   const int half = p.rotary_dim / 2;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int c = (int)(idx % chunks);
-    const long long rh = idx / chunks;
-    const int h = (int)(rh % p.heads);
-    const long long r = rh / p.heads;
-    const int pos = p.positions[r];
-    if (pos < 0 || pos >= p.table_rows) {  // no table row for this position: leave it, report it
-      atomicOr(p.err, kDevErrBounds);
-      continue;
+  const Idx stride = (Idx)gridDim.x * blockDim.x;
+  for (Idx i0 = (Idx)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    uint4 xv[2];
+    float4 cv[2], sv[2];
+    uint4* ptr[2];
+    bool ok[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const Idx idx = i0 + (Idx)u * stride;
+      ok[u] = false;
+      if (idx < total) {
+        const Idx r = idx / per_row;
+        const int q = (int)(idx - r * per_row);
+        const int h = q / chunks, c = q - h * chunks;
+        const int pos = p.positions[r];
+        ok[u] = pos >= 0 && pos < p.table_rows;
+        if (!ok[u]) atomicOr(p.err, kDevErrBounds);  // no table row for this position: leave it, report it
+        const size_t t0 = (size_t)(ok[u] ? pos : 0) * half + c * 4;
+        ptr[u] = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.x) + ((size_t)r * p.heads + h) * p.d + c * 8);
+        xv[u] = *ptr[u];
+        cv[u] = __ldg(reinterpret_cast<const float4*>(p.cos_t + t0));
+        sv[u] = __ldg(reinterpret_cast<const float4*>(p.sin_t + t0));
+      }
     }
-    uint4* ptr = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.x) + (r * p.heads + h) * p.d + c * 8);
-    const float4 cc = *reinterpret_cast<const float4*>(p.cos_t + (size_t)pos * half + c * 4);
-    const float4 ss = *reinterpret_cast<const float4*>(p.sin_t + (size_t)pos * half + c * 4);
-    *ptr = rope_rotate4(*ptr, cc, ss);
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (ok[u]) *ptr[u] = rope_rotate4(xv[u], cv[u], sv[u]);
   }
 }
 
@@ -95,10 +111,12 @@ cudaError_t launch_rope(const RopeParams& p, int sm_count, cudaStream_t stream) 
     fa_rope_rows_kernel<<<(unsigned)blocks, kRopeThreads, 0, stream>>>(p);
   } else {
     const long long total = (long long)p.rows * per_row;
-    long long blocks = (total + 255) / 256;
-    const long long cap = (long long)sm_count * 8;  // grid-stride beyond a few waves
+    long long blocks = (total + 511) / 512;
+    const long long cap = (long long)sm_count * 6;  // CTAs resident at once (registers), grid-stride beyond
     if (blocks > cap) blocks = cap;
-    fa_rope_flat_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    // 32-bit indices while the index plus two grid strides stays below 2^32
+    if (total < (1ll << 31)) fa_rope_flat_kernel<uint32_t><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else fa_rope_flat_kernel<long long><<<(unsigned)blocks, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
