@@ -49,6 +49,29 @@ def test_alibi_prefill_matches_oracle(case):
     assert fa.fa_device_status() == 0
 
 
+def test_alibi_llama7b_causal_full_size_every_row():
+    # llama7b_causal with ALiBi, launched as the bench's ALiBi row launches it, every output row
+    # against the oracle with the same slopes: the reverse walk, the chunk-bounded base of the
+    # diagonal tile and the max-free later tiles across all 1,024 persistent items.  ALiBi makes
+    # many rows follow one nearby key, so |O| reaches ~4.3 (a single V row), where bf16's half
+    # spacing is 1.56e-2: no bf16 output meets the 1e-2 side of the rule there, and the derived
+    # per-element bound (bf16 output and weight rounding) applies, as for other large-|O| cases.
+    import flashattention_forward_fa_gb300 as fa
+    from fa_workloads import LLAMA7B_CAUSAL
+    from tests._util import prefill_parity_all_rows
+    case = LLAMA7B_CAUSAL
+    x = make_prefill(case)
+    slopes = _slopes(case.Hq)
+    o, lse = fa.fa_fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), causal=True, scale=case.softmax_scale,
+                       alibi_slopes=slopes)
+    torch.cuda.synchronize()
+    res = prefill_parity_all_rows(x, o, lse, case.name + "_alibi", strict=False,
+                                  alibi_slopes=slopes.astype(np.float64))
+    assert res["rows"] == case.B * case.Hq * case.Nq and res["empty_rows"] == 0
+    assert res["o_bound_ratio"] <= 1.0
+    assert fa.fa_device_status() == 0
+
+
 def test_alibi_zero_slopes_equal_plain_prefill():
     import flashattention_forward_fa_gb300 as fa
     x = make_prefill(PrefillCase("z", B=1, Hq=4, Hkv=4, Nq=400, Nk=400, d=128, causal=True, seed=406))
