@@ -351,10 +351,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // RoPE on four packed bf16 pairs: (x, y) -> (x c - y s, x s + y c) per pair, fp32 math,
-// bf16 round-to-nearest-even result (the rotation of adjacent dimension pairs).
+// bf16 round-to-nearest-even result (the rotation of adjacent dimension pairs).  The products
+// y s and y c are split into their fp32 rounding p and its exact error e = fma(y, s, -p), so that
+// x c - y s = fma(x, c, -p) - e is off the exact value by about one fp32 rounding of the result
+// itself (<= ~2^-23 |r|), also where the two products nearly cancel; the bf16 result is then the
+// single rounding of the exact rotation except within ~2^-23 |r| of a rounding boundary.
 __device__ __forceinline__ uint32_t rope_rotate_pair(uint32_t pr, float cc, float ss) {
   const float x = __uint_as_float(pr << 16), y = __uint_as_float(pr & 0xffff0000u);
-  return pack_bf16x2(fmaf(x, cc, -y * ss), fmaf(x, ss, y * cc));
+  const float ps = __fmul_rn(y, ss), es = __fmaf_rn(y, ss, -ps);
+  const float pc = __fmul_rn(y, cc), ec = __fmaf_rn(y, cc, -pc);
+  return pack_bf16x2(__fsub_rn(__fmaf_rn(x, cc, -ps), es), __fadd_rn(__fmaf_rn(x, ss, pc), ec));
 }
 __device__ __forceinline__ uint4 rope_rotate4(uint4 w, float4 c, float4 s) {
   return make_uint4(rope_rotate_pair(w.x, c.x, s.x), rope_rotate_pair(w.y, c.y, s.y),
