@@ -85,8 +85,14 @@ def test_four_new_tokens_decode_cache_full_size_every_row():
     ro, rl = oracle.attention_rows(bf16_bits(q), bf16_bits(x.k_cache), bf16_bits(x.v_cache),
                                    [b * nt for b in range(c.B)], [nt] * c.B, [b * c.Ncap for b in range(c.B)],
                                    x.lens, c.softmax_scale, True, 0, rows)
-    go = o.float().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]].astype(np.float64)
-    gl = lse.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]].astype(np.float64)
-    res = check(go, gl, ro, rl, "decode_cache, 4 new tokens")
-    assert res["rows"] == c.B * c.Hq * nt and res["o_loose_elems"] == 0
+    # the same tokens through the prefill kernel (padded layout, per-sequence key lengths), as the
+    # bench's comparison row runs them
+    o2, lse2 = fa.fa_fwd(q.cuda(), x.k_cache.cuda(), x.v_cache.cuda(), causal=True, scale=c.softmax_scale,
+                         seqlens_k=lens)
+    torch.cuda.synchronize()
+    for out, l, what in ((o, lse, "decode kernel"), (o2, lse2, "prefill kernel")):
+        go = out.float().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]].astype(np.float64)
+        gl = l.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]].astype(np.float64)
+        res = check(go, gl, ro, rl, "decode_cache, 4 new tokens, " + what)
+        assert res["rows"] == c.B * c.Hq * nt and res["o_loose_elems"] == 0
     assert fa.fa_device_status() == 0
