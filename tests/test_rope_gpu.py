@@ -134,11 +134,12 @@ def test_fused_rope_prefill_matches_oracle(case, rd):
     assert fa.fa_device_status() == 0
 
 
-def _near_boundary(x_bf16: torch.Tensor, exact: np.ndarray, rd: int):
+def _near_boundary(x_bf16: torch.Tensor, exact: np.ndarray, rd: int, widen: float = 1.0):
     """Elements of a rotation whose exact value lies so close to a bf16 rounding boundary that the
     kernel's fp32 arithmetic (within 2^-22 |r| + 2^-46 (|x| + |y|) of it, see the tolerance above)
     may round it to the other neighbour: a mask over the rotated dimensions and the bf16 spacing
-    there (the size of such a flip)."""
+    there (the size of such a flip).  ``widen`` scales the margin (the CPU check of the allowance
+    uses a wide one so that a small problem has many such elements)."""
     x64 = x_bf16.to(torch.float64).numpy()
     ex = exact[..., :rd]
     rv = (orope.bf16_round_bits(exact)[..., :rd].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
@@ -146,12 +147,12 @@ def _near_boundary(x_bf16: torch.Tensor, exact: np.ndarray, rd: int):
     above = np.abs(ex) >= np.abs(rv)
     hr = np.ldexp(1.0, np.maximum(er, -125) - np.where((mr == 0.5) & ~above, 10, 9))
     pair = np.abs(x64[..., :rd:2]) + np.abs(x64[..., 1:rd:2])
-    delta = np.ldexp(np.abs(ex), -22) + np.ldexp(np.repeat(pair, 2, axis=-1), -46)
+    delta = widen * (np.ldexp(np.abs(ex), -22) + np.ldexp(np.repeat(pair, 2, axis=-1), -46))
     near = np.abs(ex - rv) + delta >= hr
     return near, 2.0 * np.ldexp(1.0, np.maximum(er, -125) - 9)   # a flip moves by at most one spacing
 
 
-def _rope_flip_allowance(x, qr, kr, q_ex, k_ex, rd, scale, lse_ref):
+def _rope_flip_allowance(x, qr, kr, q_ex, k_ex, rd, scale, lse_ref, widen: float = 1.0, max_frac: float = 1e-4):
     """[N, H] bound on how far the LSE of causal row i of head h (one sequence, Hq = Hkv) may move
     when boundary elements of the rotated Q and K round to their other neighbour.  Row i's scores
     change by ds_j = x_j + y_j: x_j = scale dq . k_j from its own flips dq, y_j from key j's flips
@@ -161,9 +162,9 @@ def _rope_flip_allowance(x, qr, kr, q_ex, k_ex, rd, scale, lse_ref):
     attention weights (E_p k is the oracle's attention of the row over K as values)."""
     c = x.case
     q3, k3 = x.q.reshape(-1, c.Hq, c.d), x.k.reshape(-1, c.Hkv, c.d)
-    nq, sq = _near_boundary(q3, q_ex, rd)
-    nk, sk = _near_boundary(k3, k_ex, rd)
-    assert nq.mean() < 1e-4 and nk.mean() < 1e-4
+    nq, sq = _near_boundary(q3, q_ex, rd, widen)
+    nk, sk = _near_boundary(k3, k_ex, rd, widen)
+    assert nq.mean() < max_frac and nk.mean() < max_frac
     qv = qr.to(torch.float64).numpy()
     kv = kr.to(torch.float64).numpy()
     qa = np.abs(qv[..., :rd]) + sq   # |q| after a possible flip
